@@ -1,0 +1,166 @@
+"""ctypes binding of liba4w4.so: the C ABI of include/a4w4.h, name for name.
+
+Argument marshalling only.  Tensors (torch) are passed by ``data_ptr()`` and
+must be contiguous; an ``int`` is taken as a raw pointer; ``stream=None``
+means torch's current CUDA stream.  A non-zero return code raises
+``A4W4Error``.  There is no fallback: if the library is not built the first
+call raises.
+"""
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "liba4w4.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "a4w4.h")
+
+_c_int, _c_size, _vp, _i32p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p
+
+# name -> (restype, argtypes), in the order of include/a4w4.h
+SIGNATURES = {
+    "a4w4_weight_codes_bytes": (_c_size, [_c_int, _c_int]),
+    "a4w4_weight_scales_bytes": (_c_size, [_c_int, _c_int]),
+    "a4w4_prepare_gemm_weight": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "a4w4_gemm_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_workspace_init": (_c_int, [_vp, _c_size, _vp]),
+    "a4w4_gemm": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, _vp]),
+    "a4w4_mxfp4_quant": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "a4w4_moe_w1_codes_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_moe_w1_scales_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_moe_prepare_w1": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "a4w4_moe_max_blocks": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
+    "a4w4_moe_sort_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_moe_sort": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _i32p, _vp, _c_size, _vp]),
+    "a4w4_moe_gemm1": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
+                                _vp, _vp, _vp]),
+    "a4w4_get_device_status": (_c_int, [_vp]),
+    "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
+    "a4w4_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
+}
+
+_lib = None
+
+
+class A4W4Error(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({a4w4_strerror(code)})")
+
+
+def lib():
+    """The loaded liba4w4.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(python -m mxfp4_a4w4_gemm_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor, an int pointer or None, got {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise A4W4Error(fn, rc)
+
+
+def a4w4_strerror(code):
+    return lib().a4w4_strerror(int(code)).decode()
+
+
+def a4w4_weight_codes_bytes(N, K):
+    return lib().a4w4_weight_codes_bytes(N, K)
+
+
+def a4w4_weight_scales_bytes(N, K):
+    return lib().a4w4_weight_scales_bytes(N, K)
+
+
+def a4w4_prepare_gemm_weight(W, N, K, Wq, Ws, stream=None):
+    _check("a4w4_prepare_gemm_weight",
+           lib().a4w4_prepare_gemm_weight(_ptr(W), N, K, _ptr(Wq), _ptr(Ws), _stream(stream)))
+
+
+def a4w4_gemm_workspace_bytes(M, N, K):
+    return lib().a4w4_gemm_workspace_bytes(M, N, K)
+
+
+def a4w4_workspace_init(workspace, ws_bytes, stream=None):
+    _check("a4w4_workspace_init", lib().a4w4_workspace_init(_ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def a4w4_gemm(A, M, K, Wq, Ws, N, C, workspace=None, ws_bytes=0, stream=None):
+    _check("a4w4_gemm", lib().a4w4_gemm(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C), _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
+
+
+def a4w4_mxfp4_quant(X, rows, cols, q, scales, stream=None):
+    _check("a4w4_mxfp4_quant", lib().a4w4_mxfp4_quant(_ptr(X), rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
+
+
+def a4w4_moe_w1_codes_bytes(E, two_I, D):
+    return lib().a4w4_moe_w1_codes_bytes(E, two_I, D)
+
+
+def a4w4_moe_w1_scales_bytes(E, two_I, D):
+    return lib().a4w4_moe_w1_scales_bytes(E, two_I, D)
+
+
+def a4w4_moe_prepare_w1(W1, E, two_I, D, W1q, W1s, stream=None):
+    _check("a4w4_moe_prepare_w1",
+           lib().a4w4_moe_prepare_w1(_ptr(W1), E, two_I, D, _ptr(W1q), _ptr(W1s), _stream(stream)))
+
+
+def a4w4_moe_max_blocks(T, topk, E, block_m):
+    return lib().a4w4_moe_max_blocks(T, topk, E, block_m)
+
+
+def a4w4_moe_sort_workspace_bytes(T, topk, E):
+    return lib().a4w4_moe_sort_workspace_bytes(T, topk, E)
+
+
+def a4w4_moe_sort(topk_ids, T, topk, E, block_m, sorted_rows, block_expert, num_blocks, ws, ws_bytes, stream=None):
+    _check("a4w4_moe_sort", lib().a4w4_moe_sort(_ptr(topk_ids), T, topk, E, block_m, _ptr(sorted_rows),
+                                                _ptr(block_expert), _ptr(num_blocks), _ptr(ws), ws_bytes,
+                                                _stream(stream)))
+
+
+def a4w4_moe_gemm1(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
+                   stream=None):
+    _check("a4w4_moe_gemm1", lib().a4w4_moe_gemm1(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert),
+                                                  _ptr(num_blocks), topk, _ptr(W1q), _ptr(W1s), E, I,
+                                                  _ptr(out_q), _ptr(out_s), _stream(stream)))
+
+
+def a4w4_get_device_status(stream=None):
+    """Synchronises the stream; returns (and clears) the device status code."""
+    return lib().a4w4_get_device_status(_stream(stream))
+
+
+def a4w4_set_wait_limit_ns(ns):
+    lib().a4w4_set_wait_limit_ns(int(ns))

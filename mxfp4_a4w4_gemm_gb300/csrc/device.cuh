@@ -1,0 +1,279 @@
+// device.cuh -- sm_103a primitives shared by the A4W4 kernels: mbarriers with
+// bounded waits, TMA bulk copies, tcgen05 (TMEM alloc, smem->TMEM copy,
+// block-scaled MMA, commit, TMEM loads) and the MXFP4 32-block quantiser.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace a4w4 {
+
+// Bit set in the device status word (passed to kernels by address) when a
+// bounded wait expires; read and cleared by a4w4_get_device_status().
+constexpr unsigned int kStatusTimeout = 1u;
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with parity `parity` to complete.  Gives up
+// after `limit_ns` (setting *abort and the status word) or as soon as another
+// role of the CTA has set *abort.  Returns true on success.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns, unsigned int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA bulk copy global -> shared, completion counted on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(slot_smem), "r"(cols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format, version 1).
+//   K-major, 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+  return d;
+}
+//   Scale-factor source of a 32x128b copy: 32 rows of 16 bytes, no swizzle,
+//   8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf4.block_scale: E2M1 x E2M1,
+// UE8M0 scales, both operands K-major, D in fp32, dense, M=128, MMA-K = 64.
+// sf_a/sf_b select the byte pair of the 32-bit scale words (0 or 2 with two
+// 32-blocks per MMA).
+__device__ __forceinline__ uint32_t idesc_mxf4(uint32_t n, uint32_t sf_a, uint32_t sf_b) {
+  return (sf_b << 4)            // B scale-factor id
+         | (1u << 7)            // A type E2M1
+         | (1u << 10)           // B type E2M1
+         | ((n >> 3) << 17)     // N / 8
+         | (1u << 23)           // scale type UE8M0
+         | ((128u >> 7) << 27)  // M / 128
+         | (sf_a << 29);        // A scale-factor id
+}
+
+// Copy a 128-row x 4-block scale atom (512 bytes, layout (r%32)*16+(r/32)*4+j)
+// from shared memory into 4 TMEM columns (replicated over the 4 lane groups).
+__device__ __forceinline__ void tmem_copy_sf(uint32_t taddr, uint32_t saddr) {
+  const uint64_t d = sdesc_sf(saddr);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(d) : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Arrives on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(bar) : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------------------
+// MXFP4 quantisation of one 32-element block (OCP MX rule):
+//   e = floor(log2 amax) - 2 clamped to [-127, 127]  ->  E8M0 code
+//   = max(biased_exponent(amax) - 2, 0) (BF16 and FP32 share the 8-bit
+//   exponent field, and finite amax has a biased exponent <= 254);
+//   y = |x| * 2^-e exactly (2^-e = 2^(127-code) is a normal float; a product
+//   that underflows is far below the first rounding midpoint 0.25);
+//   E2M1 by the hardware's round-to-nearest-even saturating conversion;
+//   the sign bit of x is copied, so a negative value that rounds to zero
+//   gives code 8.
+
+// Four pairs of non-negative floats -> 8 packed E2M1 codes (element 2j low nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float y0, float y1, float y2, float y3, float y4, float y5,
+                                               float y6, float y7) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(y0), "f"(y1), "f"(y2), "f"(y3), "f"(y4), "f"(y5), "f"(y6), "f"(y7));
+  return w;
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Sign bits of the 8 BF16 elements held in w[0..3] placed at bit 4i+3.
+__device__ __forceinline__ uint32_t bf16x8_signs(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+  return ((w0 >> 12) & 0x8u) | ((w0 >> 24) & 0x80u) | ((w1 >> 4) & 0x800u) | ((w1 >> 16) & 0x8000u) |
+         ((w2 << 4) & 0x80000u) | ((w2 >> 8) & 0x800000u) | ((w3 << 12) & 0x8000000u) | (w3 & 0x80000000u);
+}
+
+// x: 32 BF16 values as 16 words (element 2j in the low half of w[j]).
+// Returns the E8M0 code; codes[0..3] receive the 16 packed code bytes.
+__device__ __forceinline__ uint32_t quant32_bf16(const uint32_t* w, uint32_t* codes) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
+  const uint32_t amax = max(m & 0xFFFFu, m >> 16);
+  const uint32_t ebits = amax >> 7;
+  const uint32_t code = ebits > 2u ? ebits - 2u : 0u;
+  const float inv = __uint_as_float((254u - code) << 23);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float y[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t a = w[4 * q + j] & 0x7FFF7FFFu;
+      y[2 * j] = __uint_as_float(a << 16) * inv;
+      y[2 * j + 1] = __uint_as_float(a & 0xFFFF0000u) * inv;
+    }
+    codes[q] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]) |
+               bf16x8_signs(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+  return code;
+}
+
+// h: 32 fp32 values.  Same rule as quant32_bf16.
+__device__ __forceinline__ uint32_t quant32_f32(const float* h, uint32_t* codes) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(h[i]) & 0x7FFFFFFFu);
+  const uint32_t ebits = amax >> 23;
+  const uint32_t code = ebits > 2u ? ebits - 2u : 0u;
+  const float inv = __uint_as_float((254u - code) << 23);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float y[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t b = __float_as_uint(h[8 * q + i]);
+      y[i] = __uint_as_float(b & 0x7FFFFFFFu) * inv;
+      s |= (b >> 31) << (4 * i + 3);
+    }
+    codes[q] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]) | s;
+  }
+  return code;
+}
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+}  // namespace a4w4

@@ -1,0 +1,537 @@
+// gemm.cu -- warp-specialised tcgen05 block-scaled MXFP4 GEMM (sm_103a).
+//
+// "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Summary/Implementation:
+// BF16 activations quantised inline to MXFP4 and multiplied with preshuffled
+// MXFP4 weights on the scaled-FP4 tensor cores, BF16 direct output with M-tail
+// masking.  "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Summary: the MoE
+// GEMM1 variant emits MXFP4 codes + E8M0 scales after SwiGLU.
+//
+// One CTA computes a (weight rows) x (activation rows) tile over a K range:
+//   warp 0      TMA producer: 16 KB bulk copies of preshuffled weight tiles
+//               and their 1 KB scale atoms into a STAGES-deep smem ring;
+//   warp 1      allocates TMEM, copies each stage's scale atoms smem->TMEM
+//               (tcgen05.cp) and issues tcgen05.mma.kind::mxf4.block_scale
+//               (M=128, K=64 per instruction, 4 per 256-wide stage), then
+//               tcgen05.commit to free the stage;
+//   warps 2..   activation producers: 16-byte BF16 loads, per-32-block amax,
+//               E8M0 + E2M1 round-to-nearest-even into the 128-byte-swizzled
+//               smem operand tile and the 128x4 scale atom; the first four
+//               of them then run the epilogue (tcgen05.ld -> BF16 -> global,
+//               or split-K partials, or SwiGLU + MXFP4 requant for MoE).
+// Swap-AB (small M): the weights are the MMA's 128-row A operand and the
+// tokens its N side (16..128), so the tensor core does no work on padding
+// rows and the kernel streams weights at HBM rate; the K range is split over
+// the SMs and the last CTA of a tile sums the fp32 partials in split order.
+#include "device.cuh"
+#include "launch.h"
+
+namespace a4w4 {
+
+enum Mode { kSwap = 0, kNormal = 1, kMoe = 2 };
+
+struct GemmArgs {
+  const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
+  const uint8_t* Wq;
+  const uint8_t* Ws;
+  uint16_t* C;        // [M, N] BF16
+  float* partial;
+  unsigned int* counters;
+  int M, N, K, KT, splits, w_tiles;
+  unsigned long long wait_ns;
+  unsigned int* status;
+  // MoE GEMM1
+  const int32_t* sorted_rows;
+  const int32_t* block_expert;
+  const int32_t* num_blocks;
+  int topk, routed_rows, I, E;
+  long long expert_code_bytes, expert_sf_bytes;
+  uint8_t* out_q;
+  uint8_t* out_s;
+};
+
+template <int MODE, int NX, int STAGES>
+struct Cfg {
+  static constexpr bool kSwapAB = MODE == kSwap;
+  static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
+  static constexpr int W_ATOMS = NW / 128;
+  static constexpr int MMA_N = kSwapAB ? NX : NW;
+  static constexpr int QWARPS = (kSwapAB && NX <= 32) ? 4 : 8;   // activation producer warps
+  static constexpr int THREADS = 32 * (2 + QWARPS);
+  static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 64) ? 2 : 1;
+  static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
+  static constexpr int X_CODE_BYTES = NX * 128;
+  static constexpr int W_SF_BYTES = W_ATOMS * 1024;
+  static constexpr int X_SF_BYTES = 1024;
+  static constexpr int OFF_W = 0;
+  static constexpr int OFF_X = OFF_W + STAGES * W_CODE_BYTES;
+  static constexpr int OFF_WSF = OFF_X + STAGES * X_CODE_BYTES;
+  static constexpr int OFF_XSF = OFF_WSF + STAGES * W_SF_BYTES;
+  static constexpr int OFF_BAR = OFF_XSF + STAGES * X_SF_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 1) * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
+  static constexpr int ACC_COLS = MMA_N;
+  static constexpr int SFA_COLS = 8;                             // 2 K-atoms x 4 columns
+  static constexpr int SFB_COLS = 8 * ((MMA_N + 127) / 128);
+  static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int TMEM_NEED = ACC_COLS + STAGES * SF_STAGE_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512);
+  static constexpr int BLOCKS_PER_STAGE = NX * 8;                // (row, 32-block) pairs
+  static constexpr int PER_THREAD = (BLOCKS_PER_STAGE + QWARPS * 32 - 1) / (QWARPS * 32);
+  static_assert(NX % 16 == 0 && NX <= 128, "activation tile");
+  static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(MIN_BLOCKS * TMEM_COLS <= 512, "co-resident CTAs must fit in TMEM");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE, int NX, int STAGES>
+__global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, STAGES>::MIN_BLOCKS)
+    a4w4_gemm_kernel(const GemmArgs p) {
+  using Cf = Cfg<MODE, NX, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int w_tile = blockIdx.x;
+  const int x_tile = blockIdx.y;
+  const int split = blockIdx.z;
+
+  int expert = 0;
+  if (MODE == kMoe) {
+    if (x_tile >= *p.num_blocks) return;           // block does not exist for this routing
+    expert = p.block_expert[x_tile];
+    if (expert < 0 || expert >= p.E) return;
+  }
+  const int kt0 = static_cast<int>(static_cast<long long>(split) * p.KT / p.splits);
+  const int kt1 = static_cast<int>(static_cast<long long>(split + 1) * p.KT / p.splits);
+  const int nk = kt1 - kt0;
+
+  const uint32_t bar0 = base + Cf::OFF_BAR;
+  auto full_w = [&](int s) { return bar0 + 8u * s; };
+  auto full_x = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * STAGES + s); };
+  const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cf::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 8);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 16);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 24);
+  volatile int* epi_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_w(s), 1);
+      mbar_init(full_x(s), Cf::QWARPS * 32);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *never = 0;
+    *epi_ready = 0;
+    fence_barrier_init();
+  }
+  // Scale atoms of activation rows that are never written must hold zeros.
+  for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
+    reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- weight producer ----------------
+    if (lane == 0 && nk > 0) {
+      // Dense large-M tiles re-read each weight tile from L2 once per activation
+      // tile; swap-AB and MoE stream every weight byte once.
+      const uint64_t pol = (MODE == kNormal) ? policy_evict_last() : policy_evict_first();
+      const uint8_t* wq = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
+      const uint8_t* wsf = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
+      int i = 0;
+      for (; i < nk; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        mbar_arrive_expect_tx(full_w(s), Cf::W_ATOMS * (16384 + 1024));
+#pragma unroll
+        for (int a = 0; a < Cf::W_ATOMS; ++a) {
+          const long long atom = static_cast<long long>(w_tile * Cf::W_ATOMS + a) * p.KT + (kt0 + i);
+          bulk_g2s(base + Cf::OFF_W + s * Cf::W_CODE_BYTES + a * 16384, wq + atom * 16384, 16384, full_w(s), pol);
+          bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES + a * 1024, wsf + atom * 1024, 1024, full_w(s), pol);
+        }
+      }
+      if (*abort_flag) {
+        // Let copies already issued land before the CTA's smem is released.
+        for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j)
+          mbar_wait(full_w(j % STAGES), (j / STAGES) & 1u, never, p.wait_ns, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(full_w(s), ph, abort_flag, p.wait_ns, p.status) || !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa = tmem + Cf::ACC_COLS + s * Cf::SF_STAGE_COLS;
+        const uint32_t sfb = sfa + Cf::SFA_COLS;
+        const uint32_t w_tile_s = base + Cf::OFF_W + s * Cf::W_CODE_BYTES;
+        const uint32_t x_tile_s = base + Cf::OFF_X + s * Cf::X_CODE_BYTES;
+        const uint32_t w_sf_s = base + Cf::OFF_WSF + s * Cf::W_SF_BYTES;
+        const uint32_t x_sf_s = base + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
+        const uint32_t a_tile = Cf::kSwapAB ? w_tile_s : x_tile_s;
+        const uint32_t b_tile = Cf::kSwapAB ? x_tile_s : w_tile_s;
+        const uint32_t a_sf = Cf::kSwapAB ? w_sf_s : x_sf_s;
+        const uint32_t b_sf = Cf::kSwapAB ? x_sf_s : w_sf_s;
+#pragma unroll
+        for (int ka = 0; ka < 2; ++ka) {
+          tmem_copy_sf(sfa + ka * 4, a_sf + ka * 512);
+          if (Cf::kSwapAB) {
+            tmem_copy_sf(sfb + ka * 4, b_sf + ka * 512);
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cf::W_ATOMS; ++j) tmem_copy_sf(sfb + ka * 8 + j * 4, b_sf + j * 1024 + ka * 512);
+          }
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const int ka = ks >> 1;
+          const uint32_t sfid = (ks & 1) * 2;
+          mma_mxf4(tmem, sdesc_sw128(a_tile + ks * 32), sdesc_sw128(b_tile + ks * 32),
+                   idesc_mxf4(Cf::MMA_N, sfid, sfid), sfa + ka * 4, sfb + ka * (Cf::kSwapAB ? 4 : 8),
+                   (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(empty(s));
+      }
+      mma_commit(tmem_full);
+      // Never release TMEM while MMAs may still be running.
+      if (!ok) mbar_wait(tmem_full, 0, never, p.wait_ns, p.status);
+    }
+  } else {
+    // ---------------- activation producers ----------------
+    const int qt = threadIdx.x - 64;
+    constexpr int P = Cf::QWARPS * 32;
+    constexpr int PER = Cf::PER_THREAD;
+    const uint16_t* rowp[PER];
+    bool rvalid[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int j = qt + u * P;
+      const int r = j >> 3;
+      rowp[u] = p.A;
+      rvalid[u] = false;
+      if (j < Cf::BLOCKS_PER_STAGE) {
+        if (MODE == kMoe) {
+          const int entry = p.sorted_rows[x_tile * 128 + r];
+          if (entry >= 0 && entry < p.routed_rows) {
+            rvalid[u] = true;
+            rowp[u] = p.A + static_cast<long long>(entry / p.topk) * p.K;
+          }
+        } else {
+          const int gm = x_tile * NX + r;
+          if (gm < p.M) {
+            rvalid[u] = true;
+            rowp[u] = p.A + static_cast<long long>(gm) * p.K;
+          }
+        }
+      }
+    }
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+      const int kbase = (kt0 + i) * 256;
+      uint32_t w[PER][16];
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int j = qt + u * P;
+        const int k = kbase + (j & 7) * 32;
+        if (j < Cf::BLOCKS_PER_STAGE && rvalid[u] && k < p.K) {
+          const uint4* src = reinterpret_cast<const uint4*>(rowp[u] + k);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint4 v = ld_global_nc_v4(src + t);
+            w[u][4 * t] = v.x; w[u][4 * t + 1] = v.y; w[u][4 * t + 2] = v.z; w[u][4 * t + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w[u][t] = 0u;
+        }
+      }
+      uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
+      uint8_t* xs = smem + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int j = qt + u * P;
+        if (j < Cf::BLOCKS_PER_STAGE) {
+          const int r = j >> 3, kb = j & 7;
+          uint32_t c[4];
+          const uint32_t e = quant32_bf16(w[u], c);
+          *reinterpret_cast<uint4*>(xt + (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4)) =
+              make_uint4(c[0], c[1], c[2], c[3]);
+          xs[(kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(e);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(full_x(s));
+    }
+
+    // ---------------- epilogue (4 warps, one per TMEM lane quadrant) ----------------
+    if (warp < 6) {
+      const int q = warp & 3;
+      const int lrow = q * 32 + lane;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+      // One thread decides for all four epilogue warps, so that every named
+      // barrier below is reached by all of them or by none.
+      if (warp == 2 && lane == 0)
+        *epi_ready = (mbar_wait(tmem_full, 0, abort_flag, p.wait_ns, p.status) && !*abort_flag && nk > 0) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const int ready = *epi_ready;
+      __syncwarp();
+      tc_fence_after();
+      if (ready) {
+        if (MODE == kSwap) {
+          const int n = w_tile * 128 + lrow;
+          const int m0 = x_tile * NX;
+          const int mvalid = min(NX, p.M - m0);
+          if (p.splits == 1) {
+#pragma unroll
+            for (int c0 = 0; c0 < NX; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < mvalid) p.C[static_cast<long long>(m0 + c0 + j) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+            }
+          } else {
+            const int tile = x_tile * p.w_tiles + w_tile;
+            float* part = p.partial + (static_cast<long long>(tile) * p.splits + split) * (128 * NX);
+#pragma unroll
+            for (int c0 = 0; c0 < NX; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < mvalid) __stcg(part + (c0 + j) * 128 + lrow, v[j]);
+            }
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (warp == 2 && lane == 0) {
+              const unsigned prev = atomicAdd(p.counters + tile, 1u);
+              *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            }
+            named_bar_sync(1, 128);
+            if (*last_flag) {
+              __threadfence();
+              const float* tbase = p.partial + static_cast<long long>(tile) * p.splits * (128 * NX);
+              for (int t = 0; t < mvalid; ++t) {
+                float acc = 0.f;
+                for (int sp = 0; sp < p.splits; ++sp) acc += __ldcg(tbase + static_cast<long long>(sp) * (128 * NX) + t * 128 + lrow);
+                p.C[static_cast<long long>(m0 + t) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+              }
+              if (warp == 2 && lane == 0) p.counters[tile] = 0u;
+            }
+          }
+        } else if (MODE == kNormal) {
+          const int m = x_tile * 128 + lrow;
+          const int n0 = w_tile * 256;
+          if (p.splits == 1) {
+#pragma unroll 4
+            for (int c0 = 0; c0 < 256; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+              if (m < p.M) {
+                uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m) * p.N + n0 + c0);
+                dst[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                dst[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
+              }
+            }
+          } else {
+            const int tile = x_tile * p.w_tiles + w_tile;
+            float* part = p.partial + (static_cast<long long>(tile) * p.splits + split) * (128 * 256);
+#pragma unroll 4
+            for (int c0 = 0; c0 < 256; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+              float4* dst = reinterpret_cast<float4*>(part + lrow * 256 + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            }
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (warp == 2 && lane == 0) {
+              const unsigned prev = atomicAdd(p.counters + tile, 1u);
+              *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            }
+            named_bar_sync(1, 128);
+            if (*last_flag) {
+              __threadfence();
+              const float* tbase = p.partial + static_cast<long long>(tile) * p.splits * (128 * 256);
+              if (m < p.M) {
+                for (int c0 = 0; c0 < 256; c0 += 8) {
+                  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                  for (int sp = 0; sp < p.splits; ++sp) {
+                    const float4* src = reinterpret_cast<const float4*>(tbase + static_cast<long long>(sp) * (128 * 256) + lrow * 256 + c0);
+                    const float4 a = __ldcg(src), b = __ldcg(src + 1);
+                    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                  }
+                  *reinterpret_cast<uint4*>(p.C + static_cast<long long>(m) * p.N + n0 + c0) =
+                      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                }
+              }
+              if (warp == 2 && lane == 0) p.counters[tile] = 0u;
+            }
+          }
+        } else {  // kMoe: SwiGLU + MXFP4 requant of 128 output columns per CTA
+          const int entry = p.sorted_rows[x_tile * 128 + lrow];
+          const bool valid = entry >= 0 && entry < p.routed_rows;
+          const int jc0 = w_tile * 128;
+#pragma unroll 1
+          for (int g4 = 0; g4 < 4; ++g4) {
+            float g[32], u[32], h[32];
+            tmem_ld16(tq + g4 * 32, g);
+            tmem_ld16(tq + g4 * 32 + 16, g + 16);
+            tmem_ld16(tq + 128 + g4 * 32, u);
+            tmem_ld16(tq + 128 + g4 * 32 + 16, u + 16);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+            uint32_t c[4];
+            const uint32_t e = quant32_f32(h, c);
+            if (valid) {
+              const int col = jc0 + g4 * 32;
+              *reinterpret_cast<uint4*>(p.out_q + static_cast<long long>(entry) * (p.I / 2) + col / 2) = make_uint4(c[0], c[1], c[2], c[3]);
+              p.out_s[static_cast<long long>(entry) * (p.I / 32) + col / 32] = static_cast<uint8_t>(e);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Cf::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+template <int MODE, int NX, int STAGES>
+static int launch_cfg(const GemmArgs& a, dim3 grid, cudaStream_t st) {
+  using Cf = Cfg<MODE, NX, STAGES>;
+  auto kern = a4w4_gemm_kernel<MODE, NX, STAGES>;
+  static bool attr_done = false;   // per instantiation; benign race (idempotent)
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
+      return -4;
+    attr_done = true;
+  }
+  kern<<<grid, Cf::THREADS, Cf::SMEM_BYTES, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+static int swap_nx(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
+
+GemmPlan plan_gemm(int M, int N, int K, int sms) {
+  GemmPlan pl{};
+  pl.kt = (K + 255) / 256;
+  int ctas_per_sm;
+  size_t tile_elems;
+  if (M <= 128) {
+    pl.swap_ab = 1;
+    pl.nx = swap_nx(M);
+    pl.w_tiles = N / 128;
+    pl.x_tiles = (M + pl.nx - 1) / pl.nx;
+    ctas_per_sm = pl.nx <= 64 ? 2 : 1;
+    tile_elems = static_cast<size_t>(128) * pl.nx;
+  } else {
+    pl.swap_ab = 0;
+    pl.nx = 128;
+    pl.w_tiles = N / 256;
+    pl.x_tiles = (M + 127) / 128;
+    ctas_per_sm = 1;
+    tile_elems = static_cast<size_t>(128) * 256;
+  }
+  const int tiles = pl.w_tiles * pl.x_tiles;
+  int splits = (sms * ctas_per_sm) / (tiles > 0 ? tiles : 1);
+  if (splits > pl.kt) splits = pl.kt;
+  if (splits < 1) splits = 1;
+  pl.splits = splits;
+  if (splits > 1) {
+    pl.partial_bytes = static_cast<size_t>(tiles) * splits * tile_elems * sizeof(float);
+    pl.ws_bytes = pl.partial_bytes + ((static_cast<size_t>(tiles) * sizeof(unsigned int) + 255) & ~static_cast<size_t>(255));
+  }
+  return pl;
+}
+
+int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
+                void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
+  GemmArgs a{};
+  a.status = status;
+  a.A = static_cast<const uint16_t*>(A);
+  a.Wq = static_cast<const uint8_t*>(Wq);
+  a.Ws = static_cast<const uint8_t*>(Ws);
+  a.C = static_cast<uint16_t*>(C);
+  if (pl.splits > 1) {
+    a.partial = static_cast<float*>(ws);
+    a.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + pl.partial_bytes);
+  }
+  a.M = M; a.N = N; a.K = K; a.KT = pl.kt; a.splits = pl.splits; a.w_tiles = pl.w_tiles;
+  a.wait_ns = wait_ns;
+  const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
+  if (pl.swap_ab) {
+    switch (pl.nx) {
+      case 16: return launch_cfg<kSwap, 16, 5>(a, grid, st);
+      case 32: return launch_cfg<kSwap, 32, 5>(a, grid, st);
+      case 64: return launch_cfg<kSwap, 64, 4>(a, grid, st);
+      default: return launch_cfg<kSwap, 128, 6>(a, grid, st);
+    }
+  }
+  return launch_cfg<kNormal, 128, 4>(a, grid, st);
+}
+
+int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
+                     const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s, int E,
+                     int I, void* out_q, void* out_s, cudaStream_t st, unsigned long long wait_ns,
+                     unsigned int* status) {
+  GemmArgs a{};
+  a.status = status;
+  a.A = static_cast<const uint16_t*>(X);
+  a.Wq = static_cast<const uint8_t*>(W1q);
+  a.Ws = static_cast<const uint8_t*>(W1s);
+  a.M = T; a.N = 2 * I; a.K = D; a.KT = (D + 255) / 256; a.splits = 1; a.w_tiles = I / 128;
+  a.wait_ns = wait_ns;
+  a.sorted_rows = sorted_rows;
+  a.block_expert = block_expert;
+  a.num_blocks = num_blocks;
+  a.topk = topk;
+  a.routed_rows = T * topk;
+  a.I = I;
+  a.E = E;
+  const long long kp = static_cast<long long>(a.KT) * 256;
+  a.expert_code_bytes = static_cast<long long>(2 * I) * kp / 2;
+  a.expert_sf_bytes = static_cast<long long>(2 * I) * kp / 32;
+  a.out_q = static_cast<uint8_t*>(out_q);
+  a.out_s = static_cast<uint8_t*>(out_s);
+  if (max_blocks <= 0) return 0;
+  return launch_cfg<kMoe, 128, 4>(a, dim3(I / 128, max_blocks, 1), st);
+}
+
+}  // namespace a4w4

@@ -1,0 +1,38 @@
+// launch.h -- host-side launchers behind the C ABI (internal).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace a4w4 {
+
+// Tile plan of one dense GEMM call: a pure function of (M, N, K, SM count),
+// shared by a4w4_gemm and a4w4_gemm_workspace_bytes.
+struct GemmPlan {
+  int swap_ab;      // 1: weights are the MMA's M side (small M)
+  int nx;           // activation rows per CTA
+  int w_tiles;      // weight-row tiles (N / 128 or N / 256)
+  int x_tiles;      // activation-row tiles
+  int splits;       // K splits
+  int kt;           // 256-wide K tiles
+  size_t partial_bytes;   // fp32 split-K partial tiles
+  size_t ws_bytes;        // partial tiles + tile counters (0 without split-K)
+};
+
+GemmPlan plan_gemm(int M, int N, int K, int sms);
+
+int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms);
+int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
+                          cudaStream_t st, int sms);
+int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
+                void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
+int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
+                     const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s,
+                     int E, int I, void* out_q, void* out_s, cudaStream_t st, unsigned long long wait_ns,
+                     unsigned int* status);
+int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
+                    int32_t* block_expert, int32_t* num_blocks, void* ws, cudaStream_t st);
+size_t moe_sort_ws_bytes(int T, int topk, int E);
+
+}  // namespace a4w4

@@ -1,0 +1,67 @@
+"""The C ABI library loads and exports every symbol include/a4w4.h declares
+(CPU only: no kernel is launched), and the calls that need no GPU behave."""
+
+import os
+import re
+
+import pytest
+
+import mxfp4_a4w4_gemm_gb300 as a4w4
+from mxfp4_a4w4_gemm_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return a4w4.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "a4w4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(a4w4_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported_and_bound(L):
+    names = declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in a4w4.SIGNATURES, n
+
+
+def test_size_functions():
+    assert a4w4.a4w4_weight_codes_bytes(256, 256) == 256 * 256 // 2
+    assert a4w4.a4w4_weight_codes_bytes(1536, 4224) == 1536 * 4352 // 2          # K padded to 256
+    assert a4w4.a4w4_weight_scales_bytes(1536, 4224) == 1536 * 4352 // 32
+    assert a4w4.a4w4_moe_w1_codes_bytes(896, 1536, 3584) == 896 * 1536 * 3584 // 2
+    assert a4w4.a4w4_moe_max_blocks(4096, 16, 896, 128) == 512 + 896
+    assert a4w4.a4w4_moe_max_blocks(1, 16, 896, 128) == 1 + 16
+    assert a4w4.a4w4_gemm_workspace_bytes(2048, 8448, 7168) == 0                  # no split-K there
+    assert a4w4.a4w4_gemm_workspace_bytes(1, 1536, 7168) > 0
+
+
+def test_argument_errors_need_no_device():
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_gemm(16, 1, 256, 16, 16, 300, 16, stream=0)        # N % 256 != 0
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_gemm(16, 1, 200, 16, 16, 256, 16, stream=0)        # K % 128 != 0
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_gemm(8, 1, 256, 16, 16, 256, 16, stream=0)         # misaligned A
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_mxfp4_quant(16, 4, 48, 16, 16, stream=0)           # cols % 32 != 0
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_moe_sort(16, 4, 2, 8, 48, 16, 16, 16, 16, 1 << 20, stream=0)   # block_m
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+
+
+def test_strerror():
+    assert a4w4.a4w4_strerror(0) == "ok"
+    for c in (-1, -2, -3, -4, -5):
+        assert a4w4.a4w4_strerror(c) != "unknown error"

@@ -1,0 +1,127 @@
+"""GPU parity: the dense A4W4 GEMM against the oracle, element by element,
+with |C - ref| <= 2^-8 |ref| + 2^-20 sum|a w| (float64 ref, before rounding)."""
+
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_a4w4_gemm_gb300 as a4w4
+import workloads
+from gpu_util import dev_bits, gemm_violations, host_bits
+from oracle import gemm
+
+pytestmark = pytest.mark.gpu
+
+GUARD_ROWS = 3
+CANARY = 0x7FC1        # a NaN pattern that the GEMM never writes
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mxfp4_a4w4_gemm_gb300 import build
+    build.build()
+    a4w4.lib()
+
+
+class Prepared:
+    def __init__(self, W_bits):
+        self.N, self.K = W_bits.shape
+        self.Wq = torch.empty(a4w4.a4w4_weight_codes_bytes(self.N, self.K), dtype=torch.uint8, device="cuda")
+        self.Ws = torch.empty(a4w4.a4w4_weight_scales_bytes(self.N, self.K), dtype=torch.uint8, device="cuda")
+        a4w4.a4w4_prepare_gemm_weight(dev_bits(W_bits), self.N, self.K, self.Wq, self.Ws)
+
+
+def run_gemm(A_bits, prep, ws=None):
+    M, K = A_bits.shape
+    N = prep.N
+    ws_bytes = a4w4.a4w4_gemm_workspace_bytes(M, N, K)
+    if ws is None or ws.numel() < ws_bytes:
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        a4w4.a4w4_workspace_init(ws, ws_bytes)
+    C = torch.full((M + GUARD_ROWS, N), 0, dtype=torch.int16, device="cuda")
+    C.fill_(CANARY - 0x10000 if CANARY >= 0x8000 else CANARY)
+    a4w4.a4w4_gemm(dev_bits(A_bits), M, K, prep.Wq, prep.Ws, N, C, ws, ws_bytes)
+    assert a4w4.a4w4_get_device_status() == 0
+    out = C.cpu().numpy().view(np.uint16)
+    assert np.all(out[M:] == CANARY), "rows >= M were written"
+    return out[:M], ws
+
+
+def check_full(A_bits, W_bits, prep=None):
+    prep = prep or Prepared(W_bits)
+    c, _ = run_gemm(A_bits, prep)
+    ref, abs_sum, cref = gemm.gemm_a4w4(A_bits, W_bits)
+    bad = gemm_violations(c, ref, abs_sum)
+    assert bad[0].size == 0, (f"{bad[0].size} of {c.size} outside tolerance; first (m, n): "
+                              f"{list(zip(bad[0][:5].tolist(), bad[1][:5].tolist()))}")
+    return c, cref
+
+
+def test_small_workload_full():
+    (M, N, K), = workloads.SMALL
+    A, W = workloads.dense_problem(M, N, K, "small")
+    c, cref = check_full(A, W)
+    assert np.mean(c == cref) > 0.95       # most outputs round to the same BF16
+
+
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 33, 64, 65, 100, 128, 129, 255, 300])
+def test_ragged_m_spans_tiles(M):
+    N, K = 512, 768
+    A, W = workloads.dense_problem(M, N, K, "decode", seed=M)
+    check_full(A, W)
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 256, 128), (8, 256, 384), (200, 768, 4224), (40, 1536, 4224),
+                                   (3, 2048, 2304), (130, 256, 256)])
+def test_k_tails_and_shapes(M, N, K):
+    A, W = workloads.dense_problem(M, N, K, "large", seed=K)
+    check_full(A, W)
+
+
+def test_stress_blocks_small():
+    A = workloads.stress_activation_bits(37, 4224)
+    W = workloads.weight_bits(256, 4224)
+    check_full(A, W)
+
+
+def test_deterministic_and_workspace_reuse():
+    A, W = workloads.dense_problem(8, 1536, 7168, "decode")
+    prep = Prepared(W)
+    c1, ws = run_gemm(A, prep)
+    c2, _ = run_gemm(A, prep, ws)
+    c3, _ = run_gemm(A, prep, ws)
+    assert np.array_equal(c1, c2) and np.array_equal(c2, c3)
+
+
+ALL_SHAPES = ([("decode", s) for s in workloads.DECODE_SWEEP] + [("large", s) for s in workloads.LARGE_M_SWEEP]
+              + [("stress", s) for s in workloads.TAIL_STRESS])
+
+
+@pytest.mark.parametrize("family,shape", ALL_SHAPES, ids=[f"{f}-{m}x{n}x{k}" for f, (m, n, k) in ALL_SHAPES])
+def test_full_size_sampled(family, shape):
+    """Every workload shape at full size, in the bench's launch configuration;
+    4096 random outputs plus the first and last rows checked against the oracle."""
+    M, N, K = shape
+    A, W = workloads.dense_problem(M, N, K, family)
+    c, _ = run_gemm(A, Prepared(W))
+    rng = np.random.default_rng(M * 7 + N)
+    ms = np.concatenate([rng.integers(0, M, 4096), np.zeros(N, np.int64), np.full(N, M - 1)])
+    ns = np.concatenate([rng.integers(0, N, 4096), np.arange(N), np.arange(N)])
+    ref, abs_sum, _ = gemm.gemm_a4w4_entries(A, W, ms, ns)
+    bad = gemm_violations(c[ms, ns], ref, abs_sum)[0]
+    assert bad.size == 0, f"{bad.size} sampled outputs outside tolerance, first {list(zip(ms[bad][:5], ns[bad][:5]))}"
+    assert np.all((c & 0x7F80) != 0x7F80), "NaN or Inf in the output"
+
+
+def test_argument_errors():
+    prep = Prepared(workloads.weight_bits(256, 256))
+    A = dev_bits(workloads.activation_bits(4, 256))
+    C = torch.empty((4, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_gemm(A, 4, 256, prep.Wq, prep.Ws, 300, C)
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+    ws_bytes = a4w4.a4w4_gemm_workspace_bytes(4, 256, 256)
+    if ws_bytes:
+        with pytest.raises(a4w4.A4W4Error) as e:
+            a4w4.a4w4_gemm(A, 4, 256, prep.Wq, prep.Ws, 256, C, None, 0)
+        assert e.value.code == a4w4.A4W4_ERR_WORKSPACE
