@@ -237,6 +237,9 @@ def run_ours(args, rank, world, local_rank):
     build.build()
     a4w4.lib()
     desc, shapes, family = WORKLOADS[args.workload]
+    if args.shape:
+        shapes = [tuple(int(v) for v in args.shape.split(","))]
+        desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({args.workload} inputs)"
     wl = DenseSweep(shapes, family, dev)
     nrot = wl.copies
 
@@ -481,6 +484,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -111,6 +111,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   const int kt0 = static_cast<int>(static_cast<long long>(split) * p.KT / p.splits);
   const int kt1 = static_cast<int>(static_cast<long long>(split + 1) * p.KT / p.splits);
   const int nk = kt1 - kt0;
+  // Waits that only drain work already in flight (bulk copies landing in this
+  // CTA's shared memory, MMAs reading TMEM) before the CTA releases them keep
+  // a floor of 0.1 s whatever limit the caller set for ordinary waits.
+  const unsigned long long drain_ns = p.wait_ns > 100000000ull ? p.wait_ns : 100000000ull;
 
   const uint32_t bar0 = base + Cf::OFF_BAR;
   auto full_w = [&](int s) { return bar0 + 8u * s; };
@@ -167,11 +171,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES + a * 1024, wsf + atom * 1024, 1024, full_w(s), pol);
         }
       }
-      if (*abort_flag) {
-        // Let copies already issued land before the CTA's smem is released.
-        for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j)
-          mbar_wait(full_w(j % STAGES), (j / STAGES) & 1u, never, p.wait_ns, p.status);
-      }
+      // Let every copy already issued land before the CTA's smem is released
+      // (immediate on the normal path; matters when another role gave up).
+      for (int j = (i > STAGES ? i - STAGES : 0); j < i; ++j)
+        mbar_wait(full_w(j % STAGES), (j / STAGES) & 1u, never, drain_ns, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -216,8 +219,10 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         mma_commit(empty(s));
       }
       mma_commit(tmem_full);
-      // Never release TMEM while MMAs may still be running.
-      if (!ok) mbar_wait(tmem_full, 0, never, p.wait_ns, p.status);
+      // Never release TMEM while MMAs may still be running, whichever role
+      // (this one or the epilogue) gave up.
+      mbar_wait(tmem_full, 0, never, drain_ns, p.status);
+      (void)ok;
     }
   } else {
     // ---------------- activation producers ----------------
