@@ -145,6 +145,28 @@ int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
                    void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dense A4W4 GEMM that allocates nothing (no counterpart on the source pages:
+ * it exists for callers of this library).  Same arguments and result as
+ * a4w4_gemm() minus the workspace.  For callers that cannot allocate device
+ * memory where they call the GEMM -- code under a framework allocator that owns
+ * all device memory, or a latency-critical path that cannot afford cudaMalloc's
+ * implicit synchronisation -- and so cannot hand a4w4_gemm() the split-K
+ * workspace it needs at small M.
+ *   Scratch: a fixed 16 MiB array inside the library's device image, present on
+ *   every GPU that loads the library until the process exits.  A shape whose
+ *   tile plan needs more (a4w4_gemm_workspace_bytes(M, N, K) > 16 MiB) is
+ *   refused with A4W4_ERR_WORKSPACE.
+ *   The first call on a device looks the array's device address up (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  It calls no allocator.
+ *   All calls on a GPU share the array and it keeps the last call's contents:
+ *   each call clears the tile counters it needs on `stream` first, and calls
+ *   that may run at the same time on one GPU (different streams) race on it --
+ *   serialise them. */
+int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
+                      void* C_bf16, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Synchronises `stream`, then returns and clears the device status word:
  * A4W4_OK, A4W4_ERR_TIMEOUT, or A4W4_ERR_LAUNCH if the stream reported an error. */
 int a4w4_get_device_status(void* stream);

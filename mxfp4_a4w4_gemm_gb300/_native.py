@@ -33,6 +33,7 @@ SIGNATURES = {
     "a4w4_moe_sort": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _i32p, _vp, _c_size, _vp]),
     "a4w4_moe_gemm1": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
                                 _vp, _vp, _vp]),
+    "a4w4_gemm_noalloc": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp]),
     "a4w4_get_device_status": (_c_int, [_vp]),
     "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
     "a4w4_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
@@ -155,6 +156,16 @@ def a4w4_moe_gemm1(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1
     _check("a4w4_moe_gemm1", lib().a4w4_moe_gemm1(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert),
                                                   _ptr(num_blocks), topk, _ptr(W1q), _ptr(W1s), E, I,
                                                   _ptr(out_q), _ptr(out_s), _stream(stream)))
+
+
+def a4w4_gemm_noalloc(A, M, K, Wq, Ws, N, C, stream=None):
+    """a4w4_gemm without a workspace, for callers that cannot allocate device
+    memory at the call site: split-K scratch comes from a fixed 16 MiB array in
+    the library (shapes that need more raise A4W4Error, A4W4_ERR_WORKSPACE).
+    Make the first call on a device before any CUDA graph capture; calls that
+    may overlap on one GPU share the array and must be serialised."""
+    _check("a4w4_gemm_noalloc", lib().a4w4_gemm_noalloc(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C),
+                                                         _stream(stream)))
 
 
 def a4w4_get_device_status(stream=None):

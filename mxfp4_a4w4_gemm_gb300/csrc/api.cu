@@ -70,6 +70,12 @@ size_t padded_k(int K) { return static_cast<size_t>((K + 255) / 256) * 256; }
 
 }  // namespace
 
+namespace a4w4 {
+int device_sms() { return current_device_sms(); }
+unsigned int* device_status_ptr() { return status_ptr(); }
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+}  // namespace a4w4
+
 extern "C" {
 
 size_t a4w4_weight_codes_bytes(int N, int K) {

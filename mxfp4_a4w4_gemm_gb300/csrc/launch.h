@@ -22,6 +22,13 @@ struct GemmPlan {
 
 GemmPlan plan_gemm(int M, int N, int K, int sms);
 
+// Shared by the C ABI entry points (defined in api.cu): SM count of the
+// current device if it is a compute capability 10.3 GPU, else a negative
+// A4W4 error code; device address of the status word; the current wait limit.
+int device_sms();
+unsigned int* device_status_ptr();
+unsigned long long wait_limit_ns();
+
 int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms);
 int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
                           cudaStream_t st, int sms);
