@@ -61,6 +61,8 @@ WORKLOADS = {
     "large": ("large-M dense A4W4 sweep, M in {128,512,2048} x (N,K) in {(8448,7168),(7168,4224)}",
               workloads.LARGE_M_SWEEP, "large"),
     "stress": ("tail/scale-edge stress, M in {37,513,2047}, N=1536, K=4224", workloads.TAIL_STRESS, "stress"),
+    "moe": ("grouped MoE GEMM1 A4W4 + SwiGLU + MXFP4 requant, T in {1,16,256,4096}, E=896, topk=16, D=3584, I=768",
+            [], "moe"),
 }
 
 
@@ -212,6 +214,93 @@ class DenseSweep:
         return {"M": M, "N": N, "K": K}
 
 
+class MoeSweep:
+    """Grouped MoE GEMM1 workload: for each token count T, the routed-row sort
+    and GEMM1 + SwiGLU + MXFP4 requant (E=896, topk=16, D=3584, I=768)."""
+
+    def __init__(self, dev, tokens=None):
+        import torch
+        import mxfp4_a4w4_gemm_gb300 as a4w4
+        from mxfp4_a4w4_gemm_gb300.host_prep import prepare_moe_w1_from_host
+        self.torch, self.a4w4, self.dev = torch, a4w4, dev
+        c = workloads.MOE
+        self.E, self.topk, self.D, self.I = c["experts"], c["topk"], c["model_dim"], c["inter_dim"]
+        self.tokens = list(tokens or c["tokens"])
+        self.W1q, self.W1s = prepare_moe_w1_from_host(
+            lambda e: workloads.moe_expert_weight_bits(e, 2 * self.I, self.D), self.E, 2 * self.I, self.D,
+            threads=16, device=dev)
+        # rotate routings so that the experts a small-T step touches are cold in L2
+        self.copies = 8
+        self.items = []
+        for T in self.tokens:
+            X = workloads.bits_to_torch(workloads.moe_tokens_bits(T, self.D))
+            routes = []
+            for v in range(self.copies):
+                ids = workloads.moe_topk_ids(T, self.E, self.topk, seed=2 + 1000 * v)
+                maxb = a4w4.a4w4_moe_max_blocks(T, self.topk, self.E, 128)
+                wsb = a4w4.a4w4_moe_sort_workspace_bytes(T, self.topk, self.E)
+                routes.append(dict(
+                    ids=torch.from_numpy(ids).to(dev), hits=int(np.unique(ids).size),
+                    rows=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
+                    bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
+                    nb=torch.empty(1, dtype=torch.int32, device=dev),
+                    ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
+            self.items.append(dict(
+                T=T, X=X.to(dev), X_host=X.pin_memory(), routes=routes,
+                q=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8, device=dev),
+                s=torch.empty((T * self.topk, self.I // 32), dtype=torch.uint8, device=dev),
+                q_host=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8).pin_memory(),
+                s_host=torch.empty((T * self.topk, self.I // 32), dtype=torch.uint8).pin_memory()))
+        self.shapes = [(it["T"], 2 * self.I, self.D) for it in self.items]
+        self.launches_per_step = 4 * len(self.items)      # 3 sort kernels + GEMM1 per T
+        self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
+        self.flops_per_step = sum(2 * it["T"] * self.topk * 2 * self.I * self.D for it in self.items)
+        torch.cuda.synchronize()
+
+    def item_bytes(self, i, r):
+        it = self.items[i]
+        T, hits = it["T"], it["routes"][r % self.copies]["hits"]
+        return int(hits * 2 * self.I * self.D * (1 / 2 + 1 / 32) + 2 * T * self.D + self.topk * T * (self.I // 2 + self.I // 32))
+
+    def call(self, i, r, sort=True, gemm=True):
+        it = self.items[i]
+        ro = it["routes"][(r * len(self.items) + i) % self.copies]
+        T = it["T"]
+        if sort:
+            self.a4w4.a4w4_moe_sort(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
+                                    ro["ws"], ro["wsb"])
+        if gemm:
+            self.a4w4.a4w4_moe_gemm1(it["X"], T, self.D, ro["rows"], ro["bexp"], ro["nb"], self.topk, self.W1q,
+                                     self.W1s, self.E, self.I, it["q"], it["s"])
+
+    def step(self, r):
+        for i in range(len(self.items)):
+            self.call(i, r)
+
+    def h2d(self):
+        for it in self.items:
+            it["X"].copy_(it["X_host"], non_blocking=True)
+
+    def d2h(self):
+        for it in self.items:
+            it["q_host"].copy_(it["q"], non_blocking=True)
+            it["s_host"].copy_(it["s"], non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(2 * it["T"] * self.D for it in self.items)
+
+    @property
+    def d2h_bytes(self):
+        return sum(it["T"] * self.topk * (self.I // 2 + self.I // 32) for it in self.items)
+
+    def kernel_name(self, i):
+        return "a4w4_gemm_kernel<moe,128>"
+
+    def label(self, i):
+        return {"T": self.items[i]["T"], "E": self.E, "topk": self.topk, "D": self.D, "I": self.I}
+
+
 def capture_graphs(torch, n, fn):
     graphs = []
     for r in range(n):
@@ -236,11 +325,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     build.build()
     a4w4.lib()
+    if args.weight_prefetch:
+        a4w4.a4w4_set_weight_prefetch(1)
     desc, shapes, family = WORKLOADS[args.workload]
-    if args.shape:
-        shapes = [tuple(int(v) for v in args.shape.split(","))]
-        desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({args.workload} inputs)"
-    wl = DenseSweep(shapes, family, dev)
+    if args.workload == "moe":
+        wl = MoeSweep(dev)
+    else:
+        if args.shape:
+            shapes = [tuple(int(v) for v in args.shape.split(","))]
+            desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({args.workload} inputs)"
+        wl = DenseSweep(shapes, family, dev)
     nrot = wl.copies
 
     def barrier():
@@ -296,8 +390,11 @@ def run_ours(args, rank, world, local_rank):
     # per-GEMM launch durations: one graph per shape of `nrot` back-to-back
     # launches on rotating weight copies, timed with events on this stream
     per = []
+    is_moe = isinstance(wl, MoeSweep)
     for i in range(len(wl.shapes)):
-        g = capture_graphs(torch, 1, lambda _r, i=i: [wl.call(i, rr) for rr in range(nrot)])[0]
+        # MoE: time GEMM1 alone (the sort's outputs for every routing are in place)
+        g = capture_graphs(torch, 1, lambda _r, i=i: [
+            (wl.call(i, rr, sort=False) if is_moe else wl.call(i, rr)) for rr in range(nrot)])[0]
         g.replay()
         reps = max(3, int(2000 // nrot))
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -309,8 +406,13 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         us = s0.elapsed_time(s1) * 1e3 / (reps * nrot)
         M, N, K = wl.shapes[i]
-        per.append(dict(wl.label(i), us=round(us, 3), tbs=round(gemm_bytes(M, N, K) / us / 1e6, 3),
-                        tflops=round(gemm_flops(M, N, K) / us / 1e6, 2), kernel=wl.kernel_name(i)))
+        if is_moe:
+            nbytes = sum(wl.item_bytes(i, rr) for rr in range(nrot)) / nrot
+            nflops = 2 * M * wl.topk * N * K
+        else:
+            nbytes, nflops = gemm_bytes(M, N, K), gemm_flops(M, N, K)
+        per.append(dict(wl.label(i), us=round(us, 3), tbs=round(nbytes / us / 1e6, 3),
+                        tflops=round(nflops / us / 1e6, 2), kernel=wl.kernel_name(i), bytes=int(nbytes)))
 
     peaks, peak_src = load_peaks()
     # dominant kernel: the instantiation with the largest share of the step
@@ -318,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
     for p in per:
         share.setdefault(p["kernel"], [0.0, 0, 0])
         share[p["kernel"]][0] += p["us"]
-        share[p["kernel"]][1] += gemm_bytes(p["M"], p["N"], p["K"])
+        share[p["kernel"]][1] += p["bytes"]
         share[p["kernel"]][2] += 1
     dom = max(share, key=lambda k: share[k][0])
     dom_us, dom_bytes, dom_n = share[dom]
@@ -365,7 +467,9 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": vs, "dtype": "e2m1 x e2m1 -> fp32 (bf16 in/out)",
         "data": "synthetic (seeded; no checkpoints or datasets)",
         "config": {"workload": desc, "gemms_per_step": len(wl.shapes), "graphs": "CUDA graphs, one per step",
-                   "l2": f"weights rotate over {nrot} copies ({nrot * sum(gemm_bytes(0, N, K) for N, K in wl.wq) / 1e6:.0f} MB > 2x L2)",
+                   "weight_prefetch": bool(args.weight_prefetch),
+                   "l2": (f"{nrot} routings rotate (experts touched per step differ); W1 is 2.6 GB" if is_moe else
+                          f"weights rotate over {nrot} copies ({nrot * sum(gemm_bytes(0, N, K) for N, K in wl.wq) / 1e6:.0f} MB > 2x L2)"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "per_gemm": per, "timed_regions": len(regions)},
         "roofline": roofline,
@@ -374,7 +478,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * wl.launches_per_step * len(regions),
         "clocks": clk.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not is_moe:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -485,6 +589,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family")
+    ap.add_argument("--weight-prefetch", action="store_true",
+                    help="let each GEMM stream its (static) weights before the previous kernel finishes")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -174,6 +174,17 @@ int a4w4_get_device_status(void* stream);
 /* Static, human-readable name of a return code. */
 const char* a4w4_strerror(int code);
 
+/* Weight prefetch across kernel boundaries (default off).  GEMM kernels are
+ * launched with programmatic dependent launch: a GEMM may start while the
+ * previous kernel on its stream is still running, and it waits for that kernel
+ * before touching activations, outputs or workspace.  With prefetch enabled it
+ * also starts streaming its WEIGHTS (Wq, Ws, W1q, W1s) before that wait, which
+ * hides the weight fetch latency behind the previous kernel.  Enable it only
+ * when the kernel issued just before a GEMM on the same stream does not write
+ * that GEMM's weights (weights prepared earlier and left unchanged, as in
+ * inference).  Applies to launches issued after the call. */
+void a4w4_set_weight_prefetch(int enable);
+
 /* Override the in-kernel wait limit in nanoseconds (0 restores the default of
  * 2e8 ns).  Applies to launches issued after the call; used to test that an
  * expired wait is reported rather than hanging. */

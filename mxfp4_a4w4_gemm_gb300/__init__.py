@@ -25,6 +25,7 @@ from ._native import (  # noqa: F401
     a4w4_mxfp4_quant,
     a4w4_prepare_gemm_weight,
     a4w4_set_wait_limit_ns,
+    a4w4_set_weight_prefetch,
     a4w4_strerror,
     a4w4_weight_codes_bytes,
     a4w4_weight_scales_bytes,

@@ -36,6 +36,7 @@ SIGNATURES = {
     "a4w4_gemm_noalloc": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp]),
     "a4w4_get_device_status": (_c_int, [_vp]),
     "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
+    "a4w4_set_weight_prefetch": (None, [_c_int]),
     "a4w4_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
 }
 
@@ -171,6 +172,12 @@ def a4w4_gemm_noalloc(A, M, K, Wq, Ws, N, C, stream=None):
 def a4w4_get_device_status(stream=None):
     """Synchronises the stream; returns (and clears) the device status code."""
     return lib().a4w4_get_device_status(_stream(stream))
+
+
+def a4w4_set_weight_prefetch(enable):
+    """Let GEMMs start streaming weights before the previous kernel on the
+    stream finishes (only if that kernel does not write those weights)."""
+    lib().a4w4_set_weight_prefetch(1 if enable else 0)
 
 
 def a4w4_set_wait_limit_ns(ns):

@@ -15,6 +15,7 @@ namespace {
 
 constexpr unsigned long long kDefaultWaitNs = 200000000ull;   // 0.2 s
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_weight_prefetch{0};
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_sms[kMaxDevices];      // 0 = unknown, -1 = unsupported, else SM count
@@ -74,6 +75,7 @@ namespace a4w4 {
 int device_sms() { return current_device_sms(); }
 unsigned int* device_status_ptr() { return status_ptr(); }
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int weight_prefetch() { return g_weight_prefetch.load(std::memory_order_relaxed); }
 }  // namespace a4w4
 
 extern "C" {
@@ -212,6 +214,8 @@ const char* a4w4_strerror(int code) {
     default: return "unknown error";
   }
 }
+
+void a4w4_set_weight_prefetch(int enable) { g_weight_prefetch.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 void a4w4_set_wait_limit_ns(unsigned long long ns) {
   g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);

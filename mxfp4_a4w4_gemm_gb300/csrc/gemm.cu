@@ -27,16 +27,24 @@
 
 namespace a4w4 {
 
-enum Mode { kSwap = 0, kNormal = 1, kMoe = 2 };
+// kSwap: weights x inline-quantised tokens (small M); kNormal: inline-quantised
+// rows x weights; kMoe: kNormal over gathered sorted rows with the SwiGLU +
+// requant epilogue; kPre: rows quantised beforehand into tiles, both operands
+// streamed by TMA (large M).
+enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3 };
 
 struct GemmArgs {
   const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
+  const uint8_t* Aq;  // kPre: activation tiles (weight layout), codes
+  const uint8_t* As;  // kPre: activation tiles, scales
   const uint8_t* Wq;
   const uint8_t* Ws;
   uint16_t* C;        // [M, N] BF16
   float* partial;
   unsigned int* counters;
   int M, N, K, KT, splits, w_tiles;
+  int cluster_reduce;   // 1: the `splits` CTAs of a tile form a cluster and reduce over DSMEM
+  int prefetch_w;       // 1: weights may be read before the previous grid on the stream completes
   unsigned long long wait_ns;
   unsigned int* status;
   // MoE GEMM1
@@ -49,15 +57,19 @@ struct GemmArgs {
   uint8_t* out_s;
 };
 
+constexpr int kRedStride = 260;      // floats per staged row of a 128x256 partial (1040 bytes)
+constexpr int kMaxClusterSplits = 8;  // portable cluster size
+
 template <int MODE, int NX, int STAGES>
 struct Cfg {
   static constexpr bool kSwapAB = MODE == kSwap;
   static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
-  static constexpr int QWARPS = (kSwapAB && NX <= 32) ? 4 : 8;   // activation producer warps
+  static constexpr bool kTmaA = MODE == kPre;                    // activations arrive by TMA too
+  static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer / epilogue warps
   static constexpr int THREADS = 32 * (2 + QWARPS);
-  static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 64) ? 2 : 1;
+  static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
   static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
   static constexpr int X_CODE_BYTES = NX * 128;
   static constexpr int W_SF_BYTES = W_ATOMS * 1024;
@@ -66,7 +78,10 @@ struct Cfg {
   static constexpr int OFF_X = OFF_W + STAGES * W_CODE_BYTES;
   static constexpr int OFF_WSF = OFF_X + STAGES * X_CODE_BYTES;
   static constexpr int OFF_XSF = OFF_WSF + STAGES * W_SF_BYTES;
-  static constexpr int OFF_BAR = OFF_XSF + STAGES * X_SF_BYTES;
+  // swap-AB split-K: peers push fp32 partial slices here (owner-indexed slots)
+  static constexpr int PUSH_BYTES = kSwapAB ? (NX + 8) * 512 : 0;
+  static constexpr int OFF_PUSH = OFF_XSF + STAGES * X_SF_BYTES;
+  static constexpr int OFF_BAR = OFF_PUSH + PUSH_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 1) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
   static constexpr int ACC_COLS = MMA_N;
@@ -81,6 +96,9 @@ struct Cfg {
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(MIN_BLOCKS * TMEM_COLS <= 512, "co-resident CTAs must fit in TMEM");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 233472, "co-resident CTAs must fit in shared memory");
+  static constexpr int RED_BYTES = kSwapAB ? NX * 128 * 4 : 128 * kRedStride * 4;
+  static_assert(RED_BYTES <= OFF_PUSH, "a staged split-K partial must fit in the drained ring");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -104,6 +122,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
 
   int expert = 0;
   if (MODE == kMoe) {
+    griddep_wait();                                // the sort that wrote num_blocks has finished
     if (x_tile >= *p.num_blocks) return;           // block does not exist for this routing
     expert = p.block_expert[x_tile];
     if (expert < 0 || expert >= p.E) return;
@@ -141,35 +160,69 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     fence_barrier_init();
   }
   // Scale atoms of activation rows that are never written must hold zeros.
-  for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
-    reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (!Cf::kTmaA)
+    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  __syncthreads();                                 // barriers initialised
+  // Start streaming weights before TMEM allocation: the first ring pass needs
+  // no empty-slot wait (fresh barriers).
+  const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
+  const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
+  const uint64_t pol = (MODE == kNormal || MODE == kPre) ? policy_evict_last() : policy_evict_first();
+  auto issue_stage = [&](int i) {
+    const int s = i % STAGES;
+    mbar_arrive_expect_tx(full_w(s), (Cf::W_ATOMS + (Cf::kTmaA ? 1 : 0)) * (16384 + 1024));
+    if (Cf::kTmaA) {
+      const long long atom = static_cast<long long>(x_tile) * p.KT + (kt0 + i);
+      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol);
+      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol);
+    }
+#pragma unroll
+    for (int a = 0; a < Cf::W_ATOMS; ++a) {
+      const long long atom = static_cast<long long>(w_tile * Cf::W_ATOMS + a) * p.KT + (kt0 + i);
+      bulk_g2s(base + Cf::OFF_W + s * Cf::W_CODE_BYTES + a * 16384, wq_e + atom * 16384, 16384, full_w(s), pol);
+      bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES + a * 1024, ws_e + atom * 1024, 1024, full_w(s), pol);
+    }
+  };
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // Weights are read before the grid dependency resolves only on request
+    // (the previous kernel on the stream must not write them), and never when
+    // a stage also carries activation tiles: those come from the kernel just
+    // before this one.
+    if (!p.prefetch_w || Cf::kTmaA) griddep_wait();
+    issued = nk < STAGES ? nk : STAGES;
+    for (int i = 0; i < issued; ++i) issue_stage(i);
+  }
+  // TMEM is allocated off the data path: the MMA warp allocates and signals
+  // the epilogue warps through a named barrier (arrive: non-blocking).
+  uint32_t tmem = 0;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    tc_fence_before();
+    __syncwarp();
+    tc_fence_after();
+    tmem = *tmem_slot;
+    named_bar_arrive(2, 32 + 128);
+  }
+  // The set-up above may overlap the previous grid on the stream (programmatic
+  // dependent launch); global memory is read and written only after it has
+  // completed.  The next grid may start its own set-up from here on.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ---------------- weight producer ----------------
     if (lane == 0 && nk > 0) {
       // Dense large-M tiles re-read each weight tile from L2 once per activation
-      // tile; swap-AB and MoE stream every weight byte once.
-      const uint64_t pol = (MODE == kNormal) ? policy_evict_last() : policy_evict_first();
-      const uint8_t* wq = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
-      const uint8_t* wsf = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
-      int i = 0;
+      // tile (evict-last); swap-AB and MoE stream every weight byte once.
+      int i = issued;
       for (; i < nk; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
         if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        mbar_arrive_expect_tx(full_w(s), Cf::W_ATOMS * (16384 + 1024));
-#pragma unroll
-        for (int a = 0; a < Cf::W_ATOMS; ++a) {
-          const long long atom = static_cast<long long>(w_tile * Cf::W_ATOMS + a) * p.KT + (kt0 + i);
-          bulk_g2s(base + Cf::OFF_W + s * Cf::W_CODE_BYTES + a * 16384, wq + atom * 16384, 16384, full_w(s), pol);
-          bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES + a * 1024, wsf + atom * 1024, 1024, full_w(s), pol);
-        }
+        issue_stage(i);
       }
       // Let every copy already issued land before the CTA's smem is released
       // (immediate on the normal path; matters when another role gave up).
@@ -183,7 +236,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       for (int i = 0; i < nk; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(full_w(s), ph, abort_flag, p.wait_ns, p.status) || !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status)) {
+        if (!mbar_wait(full_w(s), ph, abort_flag, p.wait_ns, p.status) ||
+            (!Cf::kTmaA && !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status))) {
           ok = false;
           break;
         }
@@ -253,12 +307,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         }
       }
     }
-    for (int i = 0; i < nk; ++i) {
-      const int s = i % STAGES;
-      const uint32_t ph = (i / STAGES) & 1;
-      if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+    // One stage's BF16 blocks of this thread -> registers (zeros outside A).
+    auto load_stage = [&](int i, uint32_t (&w)[PER][16]) {
       const int kbase = (kt0 + i) * 256;
-      uint32_t w[PER][16];
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
         const int j = qt + u * P;
@@ -275,6 +326,9 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           for (int t = 0; t < 16; ++t) w[u][t] = 0u;
         }
       }
+    };
+    // Quantise them into the stage's swizzled operand tile and scale atom.
+    auto quant_stage = [&](int s, const uint32_t (&w)[PER][16]) {
       uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
       uint8_t* xs = smem + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
 #pragma unroll
@@ -291,10 +345,37 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       }
       fence_proxy_async_smem();
       mbar_arrive(full_x(s));
+    };
+    const int nq = Cf::kTmaA ? 0 : nk;
+    if (PER <= 2) {
+      // Loads for stage i+1 are issued before stage i is quantised, so the L2
+      // latency of A overlaps the ALU work (two register buffers, unrolled by 2).
+      uint32_t wa[PER][16], wb[PER][16];
+      if (nq > 0) load_stage(0, wa);
+      for (int i = 0; i < nq; i += 2) {
+        if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        if (i + 1 < nq) load_stage(i + 1, wb);
+        quant_stage(i % STAGES, wa);
+        if (i + 1 >= nq) break;
+        const int i1 = i + 1;
+        if (!mbar_wait(empty(i1 % STAGES), ((i1 / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        if (i1 + 1 < nq) load_stage(i1 + 1, wa);
+        quant_stage(i1 % STAGES, wb);
+      }
+    } else {
+      for (int i = 0; i < nq; ++i) {
+        if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        uint32_t w[PER][16];
+        load_stage(i, w);
+        quant_stage(i % STAGES, w);
+      }
     }
 
     // ---------------- epilogue (4 warps, one per TMEM lane quadrant) ----------------
     if (warp < 6) {
+      named_bar_sync(2, 32 + 128);                 // TMEM address published by the MMA warp
+      tc_fence_after();
+      tmem = *tmem_slot;
       const int q = warp & 3;
       const int lrow = q * 32 + lane;
       const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -319,6 +400,33 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < mvalid) p.C[static_cast<long long>(m0 + c0 + j) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+            }
+          } else if (p.cluster_reduce) {
+            // Stage the fp32 partial [token][weight row] in the drained ring,
+            // then hand owner CTA o its tokens [o*U, (o+1)*U) as one contiguous
+            // slice, written with 16-byte DSMEM stores into slot [this split]
+            // of the owner's push buffer.
+            const int S = p.splits;
+            const int U = (NX + S - 1) / S;
+            float* red = reinterpret_cast<float*>(smem);
+#pragma unroll
+            for (int c0 = 0; c0 < NX; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + lrow] = v[j];
+            }
+            named_bar_sync(1, 128);
+            const int et = threadIdx.x - 64;
+            const uint32_t slot = base + Cf::OFF_PUSH + static_cast<uint32_t>(split * U * 128 * 4);
+            for (int o = 0; o < S; ++o) {
+              const int t0 = o * U;
+              const int t1 = min(t0 + U, mvalid);
+              if (t0 >= t1) break;
+              const float4* src = reinterpret_cast<const float4*>(red + t0 * 128);
+              const int n4 = (t1 - t0) * 32;
+              for (int i = et; i < n4; i += 128)
+                st_shared_cluster_v4(cluster_map_shared(slot + static_cast<uint32_t>(i * 16), static_cast<uint32_t>(o)), src[i]);
             }
           } else {
             const int tile = x_tile * p.w_tiles + w_tile;
@@ -349,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
               if (warp == 2 && lane == 0) p.counters[tile] = 0u;
             }
           }
-        } else if (MODE == kNormal) {
+        } else if (MODE == kNormal || MODE == kPre) {
           const int m = x_tile * 128 + lrow;
           const int n0 = w_tile * 256;
           if (p.splits == 1) {
@@ -362,6 +470,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
                 dst[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
                 dst[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
               }
+            }
+          } else if (p.cluster_reduce) {
+            // fp32 partial [row][col] into this CTA's (drained) ring, rows padded
+            // to 260 floats so that the warp's row-parallel stores spread over banks
+            float* red = reinterpret_cast<float*>(smem);
+#pragma unroll 4
+            for (int c0 = 0; c0 < 256; c0 += 16) {
+              float v[16];
+              tmem_ld16(tq + c0, v);
+              float4* dst = reinterpret_cast<float4*>(red + lrow * kRedStride + c0);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
           } else {
             const int tile = x_tile * p.w_tiles + w_tile;
@@ -426,6 +546,54 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
   }
 
+  if (MODE != kMoe && p.cluster_reduce) {
+    // Split-K over the cluster: every CTA has parked its fp32 partial in its
+    // own shared memory; CTA `rank` sums a disjoint slice of the tile from all
+    // peers in split order (bitwise deterministic) and writes BF16.  Every
+    // thread of every CTA reaches both cluster barriers.
+    cluster_sync_all();
+    if (warp >= 2 && warp < 6) {
+      const int et = threadIdx.x - 64;
+      const int S = p.splits;
+      const uint32_t rank = cluster_ctarank();
+      const uint32_t red = smem_u32(smem);
+      if (MODE == kSwap) {
+        // this CTA owns tokens [rank*U, rank*U + U): sum the pushed slots
+        // locally in split order
+        const int m0 = x_tile * NX;
+        const int mvalid = min(NX, p.M - m0);
+        const int n = w_tile * 128 + et;
+        const int U = (NX + S - 1) / S;
+        const float* push = reinterpret_cast<const float*>(smem + Cf::OFF_PUSH);
+        const int t0 = static_cast<int>(rank) * U;
+        const int t1 = min(t0 + U, mvalid);
+        for (int t = t0; t < t1; ++t) {
+          float acc = 0.f;
+          for (int c = 0; c < S; ++c) acc += push[(c * U + (t - t0)) * 128 + et];
+          p.C[static_cast<long long>(m0 + t) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        }
+      } else {
+        const int m0 = x_tile * 128;
+        const int rvalid = min(128, p.M - m0);
+        const int n = w_tile * 256 + 2 * et;
+        for (int r = static_cast<int>(rank); r < rvalid; r += S) {
+          const uint32_t off = red + static_cast<uint32_t>((r * kRedStride + 2 * et) * 4);
+          float ax = 0.f, ay = 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c < S) {
+              const float2 v = ld_shared_cluster_f32x2(cluster_map_shared(off, c));
+              ax += v.x;
+              ay += v.y;
+            }
+          *reinterpret_cast<uint32_t*>(p.C + static_cast<long long>(m0 + r) * p.N + n) = pack_bf16x2(ax, ay);
+        }
+      }
+    }
+    // pull mode: no CTA leaves while a peer may still read its shared memory
+    if (MODE != kSwap) cluster_sync_all();
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -448,7 +616,26 @@ static int launch_cfg(const GemmArgs& a, dim3 grid, cudaStream_t st) {
       return -4;
     attr_done = true;
   }
-  kern<<<grid, Cf::THREADS, Cf::SMEM_BYTES, st>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(Cf::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cf::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (a.cluster_reduce) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = 1;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = static_cast<unsigned>(a.splits);
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return -4;
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -464,13 +651,17 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     pl.nx = swap_nx(M);
     pl.w_tiles = N / 128;
     pl.x_tiles = (M + pl.nx - 1) / pl.nx;
-    ctas_per_sm = pl.nx <= 64 ? 2 : 1;
+    ctas_per_sm = pl.nx <= 32 ? 2 : 1;   // (NX=16 fits 3 per SM: the third slot lets the next grid start)
     tile_elems = static_cast<size_t>(128) * pl.nx;
   } else {
+    // Large M: quantise A once into 128-row tiles, then stream both operands
+    // by TMA (inline quantisation would redo A for every 256-column tile).
     pl.swap_ab = 0;
+    pl.prequant = 1;
     pl.nx = 128;
     pl.w_tiles = N / 256;
     pl.x_tiles = (M + 127) / 128;
+    pl.aq_bytes = static_cast<size_t>(pl.x_tiles) * pl.kt * (16384 + 1024);
     ctas_per_sm = 1;
     tile_elems = static_cast<size_t>(128) * 256;
   }
@@ -478,36 +669,57 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   int splits = (sms * ctas_per_sm) / (tiles > 0 ? tiles : 1);
   if (splits > pl.kt) splits = pl.kt;
   if (splits < 1) splits = 1;
+  // Swap-AB tiles always reduce inside a cluster (at most 8 splits); large-M
+  // tiles do when 8 splits are enough, else through the global workspace.
+  if (pl.swap_ab && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   pl.splits = splits;
-  if (splits > 1) {
+  pl.cluster_reduce = splits > 1 && splits <= kMaxClusterSplits;
+  // workspace: [activation tiles][fp32 split-K partials][tile counters]
+  if (splits > 1 && !pl.cluster_reduce) {
     pl.partial_bytes = static_cast<size_t>(tiles) * splits * tile_elems * sizeof(float);
     pl.ws_bytes = pl.partial_bytes + ((static_cast<size_t>(tiles) * sizeof(unsigned int) + 255) & ~static_cast<size_t>(255));
   }
+  pl.ws_bytes += pl.aq_bytes;
   return pl;
 }
 
 int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
                 void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
   GemmArgs a{};
+  a.prefetch_w = weight_prefetch();
   a.status = status;
   a.A = static_cast<const uint16_t*>(A);
   a.Wq = static_cast<const uint8_t*>(Wq);
   a.Ws = static_cast<const uint8_t*>(Ws);
   a.C = static_cast<uint16_t*>(C);
-  if (pl.splits > 1) {
-    a.partial = static_cast<float*>(ws);
-    a.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + pl.partial_bytes);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (pl.prequant) {
+    a.Aq = w8;
+    a.As = w8 + static_cast<size_t>(pl.x_tiles) * pl.kt * 16384;
+    w8 += pl.aq_bytes;
+  }
+  if (pl.splits > 1 && !pl.cluster_reduce) {
+    a.partial = reinterpret_cast<float*>(w8);
+    a.counters = reinterpret_cast<unsigned int*>(w8 + pl.partial_bytes);
   }
   a.M = M; a.N = N; a.K = K; a.KT = pl.kt; a.splits = pl.splits; a.w_tiles = pl.w_tiles;
+  a.cluster_reduce = pl.cluster_reduce;
   a.wait_ns = wait_ns;
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
   if (pl.swap_ab) {
     switch (pl.nx) {
-      case 16: return launch_cfg<kSwap, 16, 5>(a, grid, st);
-      case 32: return launch_cfg<kSwap, 32, 5>(a, grid, st);
-      case 64: return launch_cfg<kSwap, 64, 4>(a, grid, st);
-      default: return launch_cfg<kSwap, 128, 6>(a, grid, st);
+      case 16: return launch_cfg<kSwap, 16, 3>(a, grid, st);
+      case 32: return launch_cfg<kSwap, 32, 4>(a, grid, st);
+      case 64: return launch_cfg<kSwap, 64, 5>(a, grid, st);
+      default: return launch_cfg<kSwap, 128, 4>(a, grid, st);
     }
+  }
+  if (pl.prequant) {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int rc = launch_quant_activation_tiles(A, M, K, const_cast<uint8_t*>(a.Aq), const_cast<uint8_t*>(a.As), st, sms);
+    if (rc != 0) return rc;
+    return launch_cfg<kPre, 128, 4>(a, grid, st);
   }
   return launch_cfg<kNormal, 128, 4>(a, grid, st);
 }

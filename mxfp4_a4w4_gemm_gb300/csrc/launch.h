@@ -11,10 +11,13 @@ namespace a4w4 {
 // shared by a4w4_gemm and a4w4_gemm_workspace_bytes.
 struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
+  int prequant;     // 1: activations quantised once into tiles first (large M)
+  size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
   int w_tiles;      // weight-row tiles (N / 128 or N / 256)
   int x_tiles;      // activation-row tiles
   int splits;       // K splits
+  int cluster_reduce;     // 1: the splits of a tile form a cluster and reduce over DSMEM
   int kt;           // 256-wide K tiles
   size_t partial_bytes;   // fp32 split-K partial tiles
   size_t ws_bytes;        // partial tiles + tile counters (0 without split-K)
@@ -28,10 +31,13 @@ GemmPlan plan_gemm(int M, int N, int K, int sms);
 int device_sms();
 unsigned int* device_status_ptr();
 unsigned long long wait_limit_ns();
+int weight_prefetch();
 
 int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms);
 int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
                           cudaStream_t st, int sms);
+// A [M, K] -> MXFP4 in the weight tile layout (rows padded to 128 with zeros).
+int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms);
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                 void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,

@@ -64,9 +64,11 @@ int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const vo
     scratch = scratch_address();
     if (scratch == nullptr) return A4W4_ERR_LAUNCH;
     // The split-K tile counters must start at zero; a previous call (or one
-    // that timed out) may have left them otherwise.
-    if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + plan.partial_bytes, 0,
-                        plan.ws_bytes - plan.partial_bytes, st) != cudaSuccess)
+    // that timed out) may have left them otherwise.  They follow the
+    // activation tiles and the partials in the scratch layout.
+    const size_t counters = plan.aq_bytes + plan.partial_bytes;
+    if (plan.ws_bytes > counters &&
+        cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters, 0, plan.ws_bytes - counters, st) != cudaSuccess)
       return A4W4_ERR_LAUNCH;
   }
   return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, scratch, st, a4w4::wait_limit_ns(), status);

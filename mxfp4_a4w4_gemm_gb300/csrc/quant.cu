@@ -29,13 +29,14 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const uint4* __restric
   }
 }
 
-// One thread per (row, 32-block) of the padded weight [rows, KP]; writes the
+// One thread per (row, 32-block) of the padded matrix [rows, KP]; writes the
 // 16 code bytes into the 128-byte-swizzled tile and the scale byte into the
-// 128x4 scale atom (layout documented in a4w4.h).  With `pair_I` > 0 the
-// preshuffled row n of each expert is gate row 128*(n/256) + n%256 when
-// n%256 < 128, else up row pair_I + 128*(n/256) + n%256 - 128.
-__global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __restrict__ w, int rows, int K,
-                                                             int KT, int experts, int pair_I,
+// 128x4 scale atom (layout documented in a4w4.h).  Rows >= valid_rows (the
+// padding of an activation matrix to whole 128-row tiles) get zeros.  With
+// `pair_I` > 0 the preshuffled row n of each expert is gate row
+// 128*(n/256) + n%256 when n%256 < 128, else up row pair_I + 128*(n/256) + n%256 - 128.
+__global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __restrict__ w, int rows, int valid_rows,
+                                                             int K, int KT, int experts, int pair_I,
                                                              uint8_t* __restrict__ wq, uint8_t* __restrict__ ws) {
   const int kblocks = KT * 8;
   const long long total = static_cast<long long>(experts) * rows * kblocks;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __r
     }
     uint32_t c[4] = {0u, 0u, 0u, 0u};
     uint32_t code = 0;
-    if (kb * 32 < K) {
+    if (kb * 32 < K && n < valid_rows) {
       const uint4* src = reinterpret_cast<const uint4*>(w + (static_cast<long long>(e) * rows + src_row) * K + kb * 32);
       uint32_t v[16];
 #pragma unroll
@@ -90,8 +91,17 @@ int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_
   const int KT = (K + 255) / 256;
   const long long items = static_cast<long long>(experts) * rows * KT * 8;
   prepare_weight_kernel<<<grid_for(items, 256, sms, 8), 256, 0, st>>>(
-      static_cast<const uint16_t*>(w), rows, K, KT, experts, pair_I, static_cast<uint8_t*>(wq),
+      static_cast<const uint16_t*>(w), rows, rows, K, KT, experts, pair_I, static_cast<uint8_t*>(wq),
       static_cast<uint8_t*>(ws));
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms) {
+  const int KT = (K + 255) / 256;
+  const int rows = (M + 127) / 128 * 128;
+  const long long items = static_cast<long long>(rows) * KT * 8;
+  prepare_weight_kernel<<<grid_for(items, 256, sms, 8), 256, 0, st>>>(
+      static_cast<const uint16_t*>(a), rows, M, K, KT, 1, 0, static_cast<uint8_t*>(aq), static_cast<uint8_t*>(as));
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -39,8 +39,10 @@ def test_size_functions():
     assert a4w4.a4w4_moe_w1_codes_bytes(896, 1536, 3584) == 896 * 1536 * 3584 // 2
     assert a4w4.a4w4_moe_max_blocks(4096, 16, 896, 128) == 512 + 896
     assert a4w4.a4w4_moe_max_blocks(1, 16, 896, 128) == 1 + 16
-    assert a4w4.a4w4_gemm_workspace_bytes(2048, 8448, 7168) == 0                  # no split-K there
-    assert a4w4.a4w4_gemm_workspace_bytes(1, 1536, 7168) > 0
+    # large M: activations quantised once into 128-row x 256-K tiles (16 KB codes + 1 KB scales each)
+    assert a4w4.a4w4_gemm_workspace_bytes(2048, 8448, 7168) == 16 * 28 * (16384 + 1024)
+    # small M: split-K partials reduce inside a thread-block cluster, no workspace
+    assert a4w4.a4w4_gemm_workspace_bytes(1, 1536, 7168) == 0
 
 
 def test_argument_errors_need_no_device():
