@@ -207,7 +207,7 @@ class DenseSweep:
         if M <= 128:
             nx = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
             return f"a4w4_gemm_kernel<swap,{nx}>"
-        return "a4w4_gemm_kernel<normal,128>"
+        return "a4w4_gemm_kernel<prequant,128>"
 
     def label(self, i):
         M, N, K = self.shapes[i]
@@ -218,7 +218,8 @@ class MoeSweep:
     """Grouped MoE GEMM1 workload: for each token count T, the routed-row sort
     and GEMM1 + SwiGLU + MXFP4 requant (E=896, topk=16, D=3584, I=768)."""
 
-    def __init__(self, dev, tokens=None):
+    def __init__(self, dev, tokens=None, inline=False):
+        self.inline = inline
         import torch
         import mxfp4_a4w4_gemm_gb300 as a4w4
         from mxfp4_a4w4_gemm_gb300.host_prep import prepare_moe_w1_from_host
@@ -245,8 +246,11 @@ class MoeSweep:
                     bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
                     nb=torch.empty(1, dtype=torch.int32, device=dev),
                     ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
+            # quantise tokens once (workspace) unless T = 1 or inline quant is forced
+            xwsb = 0 if (T == 1 or self.inline) else a4w4.a4w4_moe_gemm1_workspace_bytes(T, self.D)
             self.items.append(dict(
-                T=T, X=X.to(dev), X_host=X.pin_memory(), routes=routes,
+                T=T, X=X.to(dev), X_host=X.pin_memory(), routes=routes, xwsb=xwsb,
+                xws=torch.empty(max(xwsb, 16), dtype=torch.uint8, device=dev) if xwsb else None,
                 q=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8, device=dev),
                 s=torch.empty((T * self.topk, self.I // 32), dtype=torch.uint8, device=dev),
                 q_host=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8).pin_memory(),
@@ -271,7 +275,7 @@ class MoeSweep:
                                     ro["ws"], ro["wsb"])
         if gemm:
             self.a4w4.a4w4_moe_gemm1(it["X"], T, self.D, ro["rows"], ro["bexp"], ro["nb"], self.topk, self.W1q,
-                                     self.W1s, self.E, self.I, it["q"], it["s"])
+                                     self.W1s, self.E, self.I, it["q"], it["s"], it["xws"], it["xwsb"])
 
     def step(self, r):
         for i in range(len(self.items)):
@@ -295,7 +299,7 @@ class MoeSweep:
         return sum(it["T"] * self.topk * (self.I // 2 + self.I // 32) for it in self.items)
 
     def kernel_name(self, i):
-        return "a4w4_gemm_kernel<moe,128>"
+        return "a4w4_gemm_kernel<moe,128>" if self.items[i]["xws"] is None else "a4w4_gemm_kernel<moe-prequant,128>"
 
     def label(self, i):
         return {"T": self.items[i]["T"], "E": self.E, "topk": self.topk, "D": self.D, "I": self.I}
@@ -329,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
         a4w4.a4w4_set_weight_prefetch(1)
     desc, shapes, family = WORKLOADS[args.workload]
     if args.workload == "moe":
-        wl = MoeSweep(dev)
+        wl = MoeSweep(dev, inline=args.moe_inline)
     else:
         if args.shape:
             shapes = [tuple(int(v) for v in args.shape.split(","))]
@@ -589,6 +593,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family")
+    ap.add_argument("--moe-inline", action="store_true", help="MoE: quantise gathered rows inline in every tile")
     ap.add_argument("--weight-prefetch", action="store_true",
                     help="let each GEMM stream its (static) weights before the previous kernel finishes")
     args = ap.parse_args()

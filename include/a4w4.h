@@ -138,11 +138,18 @@ int a4w4_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m,
  * h = silu(g) * u in fp32 (silu(g) = g / (1 + exp(-g)); no clamp, no bias,
  * top-k weights not applied), and h is requantised with the rule above:
  * out_q [T*topk, I/2] packed codes and out_s [T*topk, I/32] E8M0 bytes, row r.
- * X_bf16 [T, D]; W1q/W1s from a4w4_moe_prepare_w1. */
+ * X_bf16 [T, D]; W1q/W1s from a4w4_moe_prepare_w1.
+ * Activation quantisation: with ws == NULL and ws_bytes == 0 each GEMM tile
+ * quantises its gathered rows inline (as on the source pages).  Given a
+ * workspace of at least a4w4_moe_gemm1_workspace_bytes(T, D) bytes, the tokens
+ * are quantised once into it (codes [T, D/2] then scales [T, D/32]) and the
+ * tiles gather those rows: each token feeds topk rows times I/128 tiles, so
+ * this is the faster choice once T reaches a few tokens.  Same results. */
+size_t a4w4_moe_gemm1_workspace_bytes(int T, int D);
 int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
                    const int32_t* block_expert, const int32_t* num_blocks, int topk,
                    const void* W1q, const void* W1s, int E, int I, void* out_q, void* out_s,
-                   void* stream);
+                   void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Dense A4W4 GEMM that allocates nothing (no counterpart on the source pages:

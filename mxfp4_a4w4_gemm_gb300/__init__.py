@@ -16,6 +16,7 @@ from ._native import (  # noqa: F401
     a4w4_gemm_workspace_bytes,
     a4w4_get_device_status,
     a4w4_moe_gemm1,
+    a4w4_moe_gemm1_workspace_bytes,
     a4w4_moe_max_blocks,
     a4w4_moe_prepare_w1,
     a4w4_moe_sort,

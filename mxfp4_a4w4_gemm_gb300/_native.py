@@ -31,8 +31,9 @@ SIGNATURES = {
     "a4w4_moe_max_blocks": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "a4w4_moe_sort_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "a4w4_moe_sort": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _i32p, _vp, _c_size, _vp]),
+    "a4w4_moe_gemm1_workspace_bytes": (_c_size, [_c_int, _c_int]),
     "a4w4_moe_gemm1": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
-                                _vp, _vp, _vp]),
+                                _vp, _vp, _vp, _c_size, _vp]),
     "a4w4_gemm_noalloc": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp]),
     "a4w4_get_device_status": (_c_int, [_vp]),
     "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
@@ -152,11 +153,15 @@ def a4w4_moe_sort(topk_ids, T, topk, E, block_m, sorted_rows, block_expert, num_
                                                 _stream(stream)))
 
 
+def a4w4_moe_gemm1_workspace_bytes(T, D):
+    return lib().a4w4_moe_gemm1_workspace_bytes(T, D)
+
+
 def a4w4_moe_gemm1(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
-                   stream=None):
+                   ws=None, ws_bytes=0, stream=None):
     _check("a4w4_moe_gemm1", lib().a4w4_moe_gemm1(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert),
                                                   _ptr(num_blocks), topk, _ptr(W1q), _ptr(W1s), E, I,
-                                                  _ptr(out_q), _ptr(out_s), _stream(stream)))
+                                                  _ptr(out_q), _ptr(out_s), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def a4w4_gemm_noalloc(A, M, K, Wq, Ws, N, C, stream=None):

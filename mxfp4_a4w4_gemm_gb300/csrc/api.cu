@@ -175,9 +175,14 @@ int a4w4_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, 
                                as_stream(stream));
 }
 
+size_t a4w4_moe_gemm1_workspace_bytes(int T, int D) {
+  if (T <= 0 || D <= 0) return 0;
+  return static_cast<size_t>(T) * (D / 2) + static_cast<size_t>(T) * (D / 32);
+}
+
 int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                    const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
-                   void* out_q, void* out_s, void* stream) {
+                   void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream) {
   if (T <= 0 || D <= 0 || topk <= 0 || E <= 0 || I <= 0 || I % 128 != 0 || D % 128 != 0) return A4W4_ERR_ARG;
   if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
   if (!aligned16(X_bf16) || !aligned16(W1q) || !aligned16(W1s) || !aligned16(out_q) || out_s == nullptr ||
@@ -189,9 +194,14 @@ int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
   if (max_blocks > 65535) return A4W4_ERR_ARG;
   unsigned int* status = status_ptr();
   if (status == nullptr) return A4W4_ERR_LAUNCH;
+  void* xq = nullptr;
+  if (ws != nullptr || ws_bytes != 0) {
+    if (!aligned16(ws) || ws_bytes < a4w4_moe_gemm1_workspace_bytes(T, D)) return A4W4_ERR_WORKSPACE;
+    xq = ws;
+  }
   return a4w4::launch_moe_gemm1(X_bf16, T, D, sorted_rows, block_expert, num_blocks, max_blocks, topk, W1q, W1s,
-                                E, I, out_q, out_s, as_stream(stream), g_wait_ns.load(std::memory_order_relaxed),
-                                status);
+                                E, I, out_q, out_s, xq, as_stream(stream), g_wait_ns.load(std::memory_order_relaxed),
+                                status, sms);
 }
 
 int a4w4_get_device_status(void* stream) {

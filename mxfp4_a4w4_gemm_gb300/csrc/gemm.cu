@@ -30,8 +30,9 @@ namespace a4w4 {
 // kSwap: weights x inline-quantised tokens (small M); kNormal: inline-quantised
 // rows x weights; kMoe: kNormal over gathered sorted rows with the SwiGLU +
 // requant epilogue; kPre: rows quantised beforehand into tiles, both operands
-// streamed by TMA (large M).
-enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3 };
+// streamed by TMA (large M); kMoePre: kMoe gathering rows that were quantised
+// once beforehand (plain MXFP4 layout) instead of quantising them per tile.
+enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4 };
 
 struct GemmArgs {
   const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
@@ -67,6 +68,8 @@ struct Cfg {
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
   static constexpr bool kTmaA = MODE == kPre;                    // activations arrive by TMA too
+  static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;
+  static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
   static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer / epilogue warps
   static constexpr int THREADS = 32 * (2 + QWARPS);
   static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   const int split = blockIdx.z;
 
   int expert = 0;
-  if (MODE == kMoe) {
+  if (Cf::kMoeAny) {
     griddep_wait();                                // the sort that wrote num_blocks has finished
     if (x_tile >= *p.num_blocks) return;           // block does not exist for this routing
     expert = p.block_expert[x_tile];
@@ -159,10 +162,15 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     *epi_ready = 0;
     fence_barrier_init();
   }
-  // Scale atoms of activation rows that are never written must hold zeros.
-  if (!Cf::kTmaA)
+  // Activation rows that do not exist (beyond M, or padding of a routed
+  // block) are never written by the producers: their codes and scales are
+  // zeroed here once for every stage.
+  if (!Cf::kTmaA) {
+    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
       reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   fence_proxy_async_smem();
   __syncthreads();                                 // barriers initialised
   // Start streaming weights before TMEM allocation: the first ring pass needs
@@ -285,18 +293,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     constexpr int PER = Cf::PER_THREAD;
     const uint16_t* rowp[PER];
     bool rvalid[PER];
+    int tok[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int j = qt + u * P;
       const int r = j >> 3;
       rowp[u] = p.A;
       rvalid[u] = false;
+      tok[u] = 0;
       if (j < Cf::BLOCKS_PER_STAGE) {
-        if (MODE == kMoe) {
+        if (Cf::kMoeAny) {
           const int entry = p.sorted_rows[x_tile * 128 + r];
           if (entry >= 0 && entry < p.routed_rows) {
             rvalid[u] = true;
             rowp[u] = p.A + static_cast<long long>(entry / p.topk) * p.K;
+            tok[u] = entry / p.topk;
           }
         } else {
           const int gm = x_tile * NX + r;
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
         const int j = qt + u * P;
-        if (j < Cf::BLOCKS_PER_STAGE) {
+        if (j < Cf::BLOCKS_PER_STAGE && rvalid[u]) {
           const int r = j >> 3, kb = j & 7;
           uint32_t c[4];
           const uint32_t e = quant32_bf16(w[u], c);
@@ -347,7 +358,52 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       mbar_arrive(full_x(s));
     };
     const int nq = Cf::kTmaA ? 0 : nk;
-    if (PER <= 2) {
+    if constexpr (Cf::kGatherQ) {
+      // Rows were quantised once beforehand (codes [T, K/2], scales [T, K/32]):
+      // copy this thread's 16-byte code chunks and scale bytes of a stage into
+      // the swizzled tile and the scale atom; loads one stage ahead.
+      auto gload = [&](int i, uint4 (&c)[PER], uint32_t (&e)[PER]) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int j = qt + u * P;
+          const int kb = (kt0 + i) * 8 + (j & 7);
+          c[u] = make_uint4(0u, 0u, 0u, 0u);
+          e[u] = 0u;
+          if (j < Cf::BLOCKS_PER_STAGE && rvalid[u] && kb * 32 < p.K) {
+            c[u] = ld_global_nc_v4(p.Aq + static_cast<long long>(tok[u]) * (p.K / 2) + kb * 16);
+            e[u] = __ldg(p.As + static_cast<long long>(tok[u]) * (p.K / 32) + kb);
+          }
+        }
+      };
+      auto gstore = [&](int s, const uint4 (&c)[PER], const uint32_t (&e)[PER]) {
+        uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
+        uint8_t* xs = smem + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const int j = qt + u * P;
+          if (j < Cf::BLOCKS_PER_STAGE && rvalid[u]) {
+            const int r = j >> 3, kb = j & 7;
+            *reinterpret_cast<uint4*>(xt + (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4)) = c[u];
+            xs[(kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(e[u]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(full_x(s));
+      };
+      uint4 ca[PER], cb[PER];
+      uint32_t ea[PER], eb[PER];
+      if (nq > 0) gload(0, ca, ea);
+      for (int i = 0; i < nq; i += 2) {
+        if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        if (i + 1 < nq) gload(i + 1, cb, eb);
+        gstore(i % STAGES, ca, ea);
+        if (i + 1 >= nq) break;
+        const int i1 = i + 1;
+        if (!mbar_wait(empty(i1 % STAGES), ((i1 / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
+        if (i1 + 1 < nq) gload(i1 + 1, ca, ea);
+        gstore(i1 % STAGES, cb, eb);
+      }
+    } else if (PER <= 2) {
       // Loads for stage i+1 are issued before stage i is quantised, so the L2
       // latency of A overlaps the ALU work (two register buffers, unrolled by 2).
       uint32_t wa[PER][16], wb[PER][16];
@@ -520,7 +576,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
               if (warp == 2 && lane == 0) p.counters[tile] = 0u;
             }
           }
-        } else {  // kMoe: SwiGLU + MXFP4 requant of 128 output columns per CTA
+        } else {  // kMoe, kMoePre: SwiGLU + MXFP4 requant of 128 output columns per CTA
           const int entry = p.sorted_rows[x_tile * 128 + lrow];
           const bool valid = entry >= 0 && entry < p.routed_rows;
           const int jc0 = w_tile * 128;
@@ -546,7 +602,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
   }
 
-  if (MODE != kMoe && p.cluster_reduce) {
+  if (!Cf::kMoeAny && p.cluster_reduce) {
     // Split-K over the cluster: every CTA has parked its fp32 partial in its
     // own shared memory; CTA `rank` sums a disjoint slice of the tile from all
     // peers in split order (bitwise deterministic) and writes BF16.  Every
@@ -726,8 +782,8 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
 
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s, int E,
-                     int I, void* out_q, void* out_s, cudaStream_t st, unsigned long long wait_ns,
-                     unsigned int* status) {
+                     int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st, unsigned long long wait_ns,
+                     unsigned int* status, int sms) {
   GemmArgs a{};
   a.status = status;
   a.A = static_cast<const uint16_t*>(X);
@@ -748,6 +804,16 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
   a.out_q = static_cast<uint8_t*>(out_q);
   a.out_s = static_cast<uint8_t*>(out_s);
   if (max_blocks <= 0) return 0;
+  if (xq_ws != nullptr) {
+    // quantise every token once (plain MXFP4 layout), then gather those rows
+    uint8_t* xq = static_cast<uint8_t*>(xq_ws);
+    uint8_t* xs = xq + static_cast<size_t>(T) * (D / 2);
+    const int rc = launch_mxfp4_quant(X, T, D, xq, xs, st, sms);
+    if (rc != 0) return rc;
+    a.Aq = xq;
+    a.As = xs;
+    return launch_cfg<kMoePre, 128, 4>(a, dim3(I / 128, max_blocks, 1), st);
+  }
   return launch_cfg<kMoe, 128, 4>(a, dim3(I / 128, max_blocks, 1), st);
 }
 

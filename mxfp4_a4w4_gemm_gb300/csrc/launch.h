@@ -42,8 +42,8 @@ int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* W
                 void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s,
-                     int E, int I, void* out_q, void* out_s, cudaStream_t st, unsigned long long wait_ns,
-                     unsigned int* status);
+                     int E, int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
+                     unsigned long long wait_ns, unsigned int* status, int sms);
 int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
                     int32_t* block_expert, int32_t* num_blocks, void* ws, cudaStream_t st);
 size_t moe_sort_ws_bytes(int T, int topk, int E);

@@ -69,14 +69,20 @@ def h_error_bound(out):
     return 1.1 * np.abs(u) * dg + np.abs(s) * du + 2.0 ** -19 * np.abs(s * u) + 1e-30
 
 
-def run_gemm1(X_bits, ids, W1q, W1s, n_exp, inter):
+def run_gemm1(X_bits, ids, W1q, W1s, n_exp, inter, prequant=False):
+    """prequant: tokens quantised once into a workspace, else inline per tile."""
     T = X_bits.shape[0]
     topk = ids.shape[1]
     Dm = X_bits.shape[1]
     rows, bexp, nb = run_sort(ids, n_exp, 128)
     out_q = torch.full((T * topk, inter // 2), 0xEE, dtype=torch.uint8, device="cuda")
     out_s = torch.full((T * topk, inter // 32), 0xEE, dtype=torch.uint8, device="cuda")
-    a4w4.a4w4_moe_gemm1(dev_bits(X_bits), T, Dm, rows, bexp, nb, topk, W1q, W1s, n_exp, inter, out_q, out_s)
+    ws, wsb = None, 0
+    if prequant:
+        wsb = a4w4.a4w4_moe_gemm1_workspace_bytes(T, Dm)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    a4w4.a4w4_moe_gemm1(dev_bits(X_bits), T, Dm, rows, bexp, nb, topk, W1q, W1s, n_exp, inter, out_q, out_s,
+                        ws, wsb)
     assert a4w4.a4w4_get_device_status() == 0
     return out_q.cpu().numpy(), out_s.cpu().numpy()
 
@@ -96,7 +102,8 @@ def check_rows(q, s, X_bits, ids, expert_bits, rows, inter):
     return int((~same).sum()), int(fragile.sum())
 
 
-def test_gemm1_small():
+@pytest.mark.parametrize("prequant", [False, True])
+def test_gemm1_small(prequant):
     T, n_exp, topk, Dm, inter = 5, 6, 2, 256, 128
     X = workloads.moe_tokens_bits(T, Dm)
     ids = workloads.moe_topk_ids(T, n_exp, topk)
@@ -104,7 +111,7 @@ def test_gemm1_small():
     W1q = torch.empty(a4w4.a4w4_moe_w1_codes_bytes(n_exp, 2 * inter, Dm), dtype=torch.uint8, device="cuda")
     W1s = torch.empty(a4w4.a4w4_moe_w1_scales_bytes(n_exp, 2 * inter, Dm), dtype=torch.uint8, device="cuda")
     a4w4.a4w4_moe_prepare_w1(dev_bits(np.stack(W1)), n_exp, 2 * inter, Dm, W1q, W1s)
-    q, s = run_gemm1(X, ids, W1q, W1s, n_exp, inter)
+    q, s = run_gemm1(X, ids, W1q, W1s, n_exp, inter, prequant)
     check_rows(q, s, X, ids, lambda e: W1[e], np.arange(T * topk), inter)
 
 
@@ -113,14 +120,15 @@ def full_w1():
     return prepare_moe_w1_from_host(lambda e: workloads.moe_expert_weight_bits(e, 2 * I, D), E, 2 * I, D)
 
 
+@pytest.mark.parametrize("prequant", [False, True])
 @pytest.mark.parametrize("T", CFG["tokens"])
-def test_gemm1_workload(T, full_w1):
+def test_gemm1_workload(T, prequant, full_w1):
     """The MoE workload at full size; all routed rows for T = 1, else every
     routed row of 12 seeded-random experts."""
     W1q, W1s = full_w1
     X = workloads.moe_tokens_bits(T, D)
     ids = workloads.moe_topk_ids(T, E, TOPK)
-    q, s = run_gemm1(X, ids, W1q, W1s, E, I)
+    q, s = run_gemm1(X, ids, W1q, W1s, E, I, prequant)
     flat = ids.reshape(-1)
     if T == 1:
         rows = np.arange(T * TOPK)
