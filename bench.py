@@ -203,7 +203,9 @@ class DenseSweep:
         return sum(2 * M * N for M, N, _ in self.shapes)
 
     def kernel_name(self, i):
-        M = self.shapes[i][0]
+        M, N, _ = self.shapes[i]
+        if 64 < M <= 128 and N // 256 >= 16:
+            return "a4w4_gemm_kernel<normal,128>"
         if M <= 128:
             nx = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
             return f"a4w4_gemm_kernel<swap,{nx}>"

@@ -155,6 +155,11 @@ __device__ __forceinline__ void tmem_copy_sf(uint32_t taddr, uint32_t saddr) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(d) : "memory");
 }
 
+// Same copy with a prebuilt source descriptor (sdesc_sf of the atom's address).
+__device__ __forceinline__ void tmem_copy_sf_desc(uint32_t taddr, uint64_t d) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(d) : "memory");
+}
+
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(

@@ -70,7 +70,11 @@ struct Cfg {
   static constexpr bool kTmaA = MODE == kPre;                    // activations arrive by TMA too
   static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
-  static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer / epilogue warps
+  static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer warps
+  // epilogue warps (the first of the producer warps): MoE's SwiGLU + requant
+  // epilogue splits each TMEM lane quadrant's columns over two warps
+  static constexpr int EPI_WARPS = kMoeAny ? 8 : 4;
+  static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int THREADS = 32 * (2 + QWARPS);
   static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
   static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     __syncwarp();
     tc_fence_after();
     tmem = *tmem_slot;
-    named_bar_arrive(2, 32 + 128);
+    named_bar_arrive(2, 32 + Cf::EPI_THREADS);
   }
   // The set-up above may overlap the previous grid on the stream (programmatic
   // dependent launch); global memory is read and written only after it has
@@ -239,46 +243,57 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // One thread issues everything; the tensor pipe is in order, so the loop
+    // is kept lean: every descriptor is built once and advanced by additions.
     if (lane == 0) {
       bool ok = true;
+      const uint32_t a_tile0 = base + (Cf::kSwapAB ? Cf::OFF_W : Cf::OFF_X);
+      const uint32_t b_tile0 = base + (Cf::kSwapAB ? Cf::OFF_X : Cf::OFF_W);
+      const uint32_t a_sf0 = base + (Cf::kSwapAB ? Cf::OFF_WSF : Cf::OFF_XSF);
+      const uint32_t b_sf0 = base + (Cf::kSwapAB ? Cf::OFF_XSF : Cf::OFF_WSF);
+      constexpr uint32_t A_STAGE = Cf::kSwapAB ? Cf::W_CODE_BYTES : Cf::X_CODE_BYTES;
+      constexpr uint32_t B_STAGE = Cf::kSwapAB ? Cf::X_CODE_BYTES : Cf::W_CODE_BYTES;
+      constexpr uint32_t ASF_STAGE = Cf::kSwapAB ? Cf::W_SF_BYTES : Cf::X_SF_BYTES;
+      constexpr uint32_t BSF_STAGE = Cf::kSwapAB ? Cf::X_SF_BYTES : Cf::W_SF_BYTES;
+      const uint64_t adesc0 = sdesc_sw128(a_tile0), bdesc0 = sdesc_sw128(b_tile0);
+      const uint64_t asfd0 = sdesc_sf(a_sf0), bsfd0 = sdesc_sf(b_sf0);
+      const uint32_t idesc0 = idesc_mxf4(Cf::MMA_N, 0, 0), idesc2 = idesc_mxf4(Cf::MMA_N, 2, 2);
+      const uint32_t sf_col0 = tmem + Cf::ACC_COLS;
+      int s = 0;
+      uint32_t ph = 0;
       for (int i = 0; i < nk; ++i) {
-        const int s = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
         if (!mbar_wait(full_w(s), ph, abort_flag, p.wait_ns, p.status) ||
             (!Cf::kTmaA && !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t sfa = tmem + Cf::ACC_COLS + s * Cf::SF_STAGE_COLS;
+        const uint32_t sfa = sf_col0 + s * Cf::SF_STAGE_COLS;
         const uint32_t sfb = sfa + Cf::SFA_COLS;
-        const uint32_t w_tile_s = base + Cf::OFF_W + s * Cf::W_CODE_BYTES;
-        const uint32_t x_tile_s = base + Cf::OFF_X + s * Cf::X_CODE_BYTES;
-        const uint32_t w_sf_s = base + Cf::OFF_WSF + s * Cf::W_SF_BYTES;
-        const uint32_t x_sf_s = base + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
-        const uint32_t a_tile = Cf::kSwapAB ? w_tile_s : x_tile_s;
-        const uint32_t b_tile = Cf::kSwapAB ? x_tile_s : w_tile_s;
-        const uint32_t a_sf = Cf::kSwapAB ? w_sf_s : x_sf_s;
-        const uint32_t b_sf = Cf::kSwapAB ? x_sf_s : w_sf_s;
+        const uint64_t ad = adesc0 + ((s * A_STAGE) >> 4), bd = bdesc0 + ((s * B_STAGE) >> 4);
+        const uint64_t asd = asfd0 + ((s * ASF_STAGE) >> 4), bsd = bsfd0 + ((s * BSF_STAGE) >> 4);
 #pragma unroll
         for (int ka = 0; ka < 2; ++ka) {
-          tmem_copy_sf(sfa + ka * 4, a_sf + ka * 512);
+          tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
           if (Cf::kSwapAB) {
-            tmem_copy_sf(sfb + ka * 4, b_sf + ka * 512);
+            tmem_copy_sf_desc(sfb + ka * 4, bsd + ka * (512 >> 4));
           } else {
 #pragma unroll
-            for (int j = 0; j < Cf::W_ATOMS; ++j) tmem_copy_sf(sfb + ka * 8 + j * 4, b_sf + j * 1024 + ka * 512);
+            for (int j = 0; j < Cf::W_ATOMS; ++j)
+              tmem_copy_sf_desc(sfb + ka * 8 + j * 4, bsd + (j * 1024 + ka * 512) / 16);
           }
         }
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const int ka = ks >> 1;
-          const uint32_t sfid = (ks & 1) * 2;
-          mma_mxf4(tmem, sdesc_sw128(a_tile + ks * 32), sdesc_sw128(b_tile + ks * 32),
-                   idesc_mxf4(Cf::MMA_N, sfid, sfid), sfa + ka * 4, sfb + ka * (Cf::kSwapAB ? 4 : 8),
-                   (i > 0 || ks > 0) ? 1u : 0u);
+          mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4,
+                   sfb + ka * (Cf::kSwapAB ? 4 : 8), (i > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(empty(s));
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       mma_commit(tmem_full);
       // Never release TMEM while MMAs may still be running, whichever role
@@ -428,8 +443,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
 
     // ---------------- epilogue (4 warps, one per TMEM lane quadrant) ----------------
-    if (warp < 6) {
-      named_bar_sync(2, 32 + 128);                 // TMEM address published by the MMA warp
+    if (warp < 2 + Cf::EPI_WARPS) {
+      named_bar_sync(2, 32 + Cf::EPI_THREADS);     // TMEM address published by the MMA warp
       tc_fence_after();
       tmem = *tmem_slot;
       const int q = warp & 3;
@@ -439,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       // barrier below is reached by all of them or by none.
       if (warp == 2 && lane == 0)
         *epi_ready = (mbar_wait(tmem_full, 0, abort_flag, p.wait_ns, p.status) && !*abort_flag && nk > 0) ? 1 : 0;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, Cf::EPI_THREADS);
       const int ready = *epi_ready;
       __syncwarp();
       tc_fence_after();
@@ -535,9 +550,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
             for (int c0 = 0; c0 < 256; c0 += 16) {
               float v[16];
               tmem_ld16(tq + c0, v);
-              float4* dst = reinterpret_cast<float4*>(red + lrow * kRedStride + c0);
+              if (m < p.M) {                       // rows beyond M are never read
+                float4* dst = reinterpret_cast<float4*>(red + lrow * kRedStride + c0);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              }
             }
           } else {
             const int tile = x_tile * p.w_tiles + w_tile;
@@ -580,15 +597,16 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           const int entry = p.sorted_rows[x_tile * 128 + lrow];
           const bool valid = entry >= 0 && entry < p.routed_rows;
           const int jc0 = w_tile * 128;
+          const int half = (warp - 2) >> 2;           // which 64 of the 128 output columns
 #pragma unroll 1
-          for (int g4 = 0; g4 < 4; ++g4) {
+          for (int g4 = 2 * half; g4 < 2 * half + 2; ++g4) {
             float g[32], u[32], h[32];
             tmem_ld16(tq + g4 * 32, g);
             tmem_ld16(tq + g4 * 32 + 16, g + 16);
             tmem_ld16(tq + 128 + g4 * 32, u);
             tmem_ld16(tq + 128 + g4 * 32 + 16, u + 16);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+            for (int i = 0; i < 32; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
             uint32_t c[4];
             const uint32_t e = quant32_f32(h, c);
             if (valid) {
@@ -702,7 +720,16 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   pl.kt = (K + 255) / 256;
   int ctas_per_sm;
   size_t tile_elems;
-  if (M <= 128) {
+  if (M > 64 && M <= 128 && N / 256 >= 16) {
+    // tokens on the MMA's 128-row side, weights on N = 256: fewer tensor-pipe
+    // instructions per weight byte than swap-AB once M passes 64
+    pl.swap_ab = 0;
+    pl.nx = 128;
+    pl.w_tiles = N / 256;
+    pl.x_tiles = 1;
+    ctas_per_sm = 1;
+    tile_elems = static_cast<size_t>(128) * 256;
+  } else if (M <= 128) {
     pl.swap_ab = 1;
     pl.nx = swap_nx(M);
     pl.w_tiles = N / 128;
@@ -727,7 +754,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   if (splits < 1) splits = 1;
   // Swap-AB tiles always reduce inside a cluster (at most 8 splits); large-M
   // tiles do when 8 splits are enough, else through the global workspace.
-  if (pl.swap_ab && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
+  if ((pl.swap_ab || M <= 128) && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   pl.splits = splits;
   pl.cluster_reduce = splits > 1 && splits <= kMaxClusterSplits;
   // workspace: [activation tiles][fp32 split-K partials][tile counters]

@@ -125,3 +125,12 @@ def test_argument_errors():
         with pytest.raises(a4w4.A4W4Error) as e:
             a4w4.a4w4_gemm(A, 4, 256, prep.Wq, prep.Ws, 256, C, None, 0)
         assert e.value.code == a4w4.A4W4_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("M", [65, 100, 128])
+def test_mid_m_normal_orientation(M):
+    """64 < M <= 128 with N >= 4096: tokens on the MMA's 128-row side, weights
+    on N = 256, split-K reduced inside a cluster."""
+    N, K = 4096, 1792
+    A, W = workloads.dense_problem(M, N, K, "decode", seed=M + 1)
+    check_full(A, W)
