@@ -203,7 +203,10 @@ class DenseSweep:
         return sum(2 * M * N for M, N, _ in self.shapes)
 
     def kernel_name(self, i):
-        M, N, _ = self.shapes[i]
+        M, N, K = self.shapes[i]
+        if M <= 16:
+            kt = (K + 255) // 256
+            return f"a4w4_decode_kernel<16,{3 if (kt + 2) // 3 <= 8 else 4}>"
         if 64 < M <= 128 and N // 256 >= 16:
             return "a4w4_gemm_kernel<normal,128>"
         if M <= 128:
@@ -596,8 +599,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family")
     ap.add_argument("--moe-inline", action="store_true", help="MoE: quantise gathered rows inline in every tile")
-    ap.add_argument("--weight-prefetch", action="store_true",
-                    help="let each GEMM stream its (static) weights before the previous kernel finishes")
+    ap.add_argument("--no-weight-prefetch", dest="weight_prefetch", action="store_false",
+                    help="do not let a GEMM stream its weights before the previous kernel finishes (default: "
+                         "it may, since the weights are prepared before the timed region and never written in it)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

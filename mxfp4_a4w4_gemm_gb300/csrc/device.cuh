@@ -305,6 +305,49 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// Split cluster barrier: arrive early (relaxed; mbarrier inits are published
+// by fence_barrier_init), wait before the first access to a peer's memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+// 16-byte store into a peer CTA's shared memory whose completion is counted
+// (complete_tx, release at cluster scope) on an mbarrier of that same peer;
+// `dst` and `bar` are shared::cluster addresses from cluster_map_shared.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier in a peer CTA's shared
+// memory (`remote` from cluster_map_shared).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(remote) : "memory");
+}
+// Wait (acquire, cluster scope) for a phase of a local mbarrier that peers
+// arrive on; bounded like mbar_wait (no abort flag: the caller must not leave
+// before the peers' writes have landed unless the limit passes).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  unsigned int* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
 __device__ __forceinline__ uint32_t cluster_map_shared(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
@@ -318,6 +361,12 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 __device__ __forceinline__ float2 ld_shared_cluster_f32x2(uint32_t addr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {

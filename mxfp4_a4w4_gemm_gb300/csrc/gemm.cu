@@ -99,6 +99,7 @@ struct Cfg {
   static constexpr int TMEM_COLS = TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512);
   static constexpr int BLOCKS_PER_STAGE = NX * 8;                // (row, 32-block) pairs
   static constexpr int PER_THREAD = (BLOCKS_PER_STAGE + QWARPS * 32 - 1) / (QWARPS * 32);
+  static constexpr int A_DEPTH = PER_THREAD == 1 ? 4 : 2;        // stages of A loads in flight per thread
   static_assert(NX % 16 == 0 && NX <= 128, "activation tile");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(MIN_BLOCKS * TMEM_COLS <= 512, "co-resident CTAs must fit in TMEM");
@@ -419,19 +420,27 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         gstore(i1 % STAGES, cb, eb);
       }
     } else if (PER <= 2) {
-      // Loads for stage i+1 are issued before stage i is quantised, so the L2
-      // latency of A overlaps the ALU work (two register buffers, unrolled by 2).
-      uint32_t wa[PER][16], wb[PER][16];
-      if (nq > 0) load_stage(0, wa);
-      for (int i = 0; i < nq; i += 2) {
-        if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        if (i + 1 < nq) load_stage(i + 1, wb);
-        quant_stage(i % STAGES, wa);
-        if (i + 1 >= nq) break;
-        const int i1 = i + 1;
-        if (!mbar_wait(empty(i1 % STAGES), ((i1 / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        if (i1 + 1 < nq) load_stage(i1 + 1, wa);
-        quant_stage(i1 % STAGES, wb);
+      // A register ring: the loads of stages i+1 .. i+R-1 are in flight while
+      // stage i is quantised, so a CTA pays the L2 latency of A about once,
+      // not once per stage or two.
+      constexpr int R = Cf::A_DEPTH;
+      uint32_t wr[R][PER][16];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r < nq) load_stage(r, wr[r]);
+      bool stop = false;
+      for (int i0 = 0; i0 < nq && !stop; i0 += R) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int i = i0 + r;
+          if (i >= nq) break;
+          if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) {
+            stop = true;
+            break;
+          }
+          quant_stage(i % STAGES, wr[r]);
+          if (i + R < nq) load_stage(i + R, wr[r]);
+        }
       }
     } else {
       for (int i = 0; i < nq; ++i) {
@@ -729,12 +738,30 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     pl.x_tiles = 1;
     ctas_per_sm = 1;
     tile_elems = static_cast<size_t>(128) * 256;
+  } else if (M <= 16) {
+    // Decode kernel (decode.cu): the fewest K splits that let every CTA hold
+    // its whole K range in its weight ring (all its weight copies in flight
+    // at once), at most 8 (portable cluster size); no workspace.  A 3-deep
+    // ring keeps three CTAs per SM (room for the next grid's CTAs to start
+    // early and stream their weights); 4 deep when 3 would need over 8 splits.
+    pl.swap_ab = 1;
+    pl.decode = 1;
+    pl.nx = 16;
+    pl.w_tiles = N / 128;
+    pl.x_tiles = 1;
+    pl.ring = (pl.kt + 2) / 3 <= kMaxClusterSplits ? 3 : 4;
+    int splits = (pl.kt + pl.ring - 1) / pl.ring;
+    if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
+    if (splits < 1) splits = 1;
+    pl.splits = splits;
+    pl.cluster_reduce = splits > 1;
+    return pl;
   } else if (M <= 128) {
     pl.swap_ab = 1;
     pl.nx = swap_nx(M);
     pl.w_tiles = N / 128;
     pl.x_tiles = (M + pl.nx - 1) / pl.nx;
-    ctas_per_sm = pl.nx <= 32 ? 2 : 1;   // (NX=16 fits 3 per SM: the third slot lets the next grid start)
+    ctas_per_sm = pl.nx <= 32 ? 2 : 1;
     tile_elems = static_cast<size_t>(128) * pl.nx;
   } else {
     // Large M: quantise A once into 128-row tiles, then stream both operands
@@ -789,6 +816,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   a.cluster_reduce = pl.cluster_reduce;
   a.wait_ns = wait_ns;
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
+  if (pl.decode) return launch_decode(pl, A, M, K, Wq, Ws, N, C, st, wait_ns, status);
   if (pl.swap_ab) {
     switch (pl.nx) {
       case 16: return launch_cfg<kSwap, 16, 3>(a, grid, st);

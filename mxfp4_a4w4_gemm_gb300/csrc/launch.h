@@ -11,12 +11,14 @@ namespace a4w4 {
 // shared by a4w4_gemm and a4w4_gemm_workspace_bytes.
 struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
+  int decode;       // 1: M <= 16, the decode kernel (decode.cu)
   int prequant;     // 1: activations quantised once into tiles first (large M)
   size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
   int w_tiles;      // weight-row tiles (N / 128 or N / 256)
   int x_tiles;      // activation-row tiles
   int splits;       // K splits
+  int ring;         // decode kernel: weight ring depth (K tiles in flight per CTA)
   int cluster_reduce;     // 1: the splits of a tile form a cluster and reduce over DSMEM
   int kt;           // 256-wide K tiles
   size_t partial_bytes;   // fp32 split-K partial tiles
@@ -40,6 +42,9 @@ int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_
 int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms);
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                 void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
+// M <= 16 (plan.decode): the decode kernel (decode.cu); no workspace.
+int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
+                  void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s,
                      int E, int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,

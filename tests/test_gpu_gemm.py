@@ -72,7 +72,9 @@ def test_ragged_m_spans_tiles(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(8, 256, 128), (8, 256, 384), (200, 768, 4224), (40, 1536, 4224),
-                                   (3, 2048, 2304), (130, 256, 256)])
+                                   (3, 2048, 2304), (130, 256, 256),
+                                   # K ranges longer than a CTA's operand rings (several fill/drain rounds)
+                                   (1, 256, 16384), (24, 512, 12288), (50, 256, 10368)])
 def test_k_tails_and_shapes(M, N, K):
     A, W = workloads.dense_problem(M, N, K, "large", seed=K)
     check_full(A, W)
@@ -134,3 +136,32 @@ def test_mid_m_normal_orientation(M):
     N, K = 4096, 1792
     A, W = workloads.dense_problem(M, N, K, "decode", seed=M + 1)
     check_full(A, W)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1536, 7168), (8, 7168, 768), (32, 1536, 4224), (512, 512, 1024)])
+def test_weight_prefetch_back_to_back(M, N, K):
+    """With weight prefetch on, each GEMM may stream its (unchanged) weights
+    before the previous kernel on the stream has finished: results of several
+    calls issued back to back, each on other weights and activations, match
+    the oracle."""
+    problems = [workloads.dense_problem(M, N, K, "decode", seed=100 + j) for j in range(3)]
+    preps = [Prepared(W) for _, W in problems]
+    torch.cuda.synchronize()
+    a4w4.a4w4_set_weight_prefetch(1)
+    try:
+        outs = []
+        ws_bytes = a4w4.a4w4_gemm_workspace_bytes(M, N, K)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        a4w4.a4w4_workspace_init(ws, ws_bytes)
+        for (A, _), prep in zip(problems, preps):
+            C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+            a4w4.a4w4_gemm(dev_bits(A), M, K, prep.Wq, prep.Ws, N, C, ws, ws_bytes)
+            outs.append(C)
+        assert a4w4.a4w4_get_device_status() == 0
+    finally:
+        a4w4.a4w4_set_weight_prefetch(0)
+    for (A, W), C in zip(problems, outs):
+        ref, abs_sum, _ = gemm.gemm_a4w4(A, W)
+        c = C.cpu().numpy().view(np.uint16)
+        bad = gemm_violations(c, ref, abs_sum)
+        assert bad[0].size == 0, f"{bad[0].size} of {c.size} outside tolerance"
