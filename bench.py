@@ -436,7 +436,7 @@ def run_ours(args, rank, world, local_rank):
     achieved_gbs = dom_bytes / (dom_us * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                "traffic": traffic_from_profiles(dom), "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": traffic_from_profiles(args.workload, dom), "peak_source": f"{peak_src} hbm_gbs",
                 "bytes_per_launch": round(dom_bytes / dom_n), "avg_launch_us": round(dom_us / dom_n, 3)}
 
     # end to end through the C ABI with host buffers
@@ -495,16 +495,18 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.destroy_process_group()
 
 
-def traffic_from_profiles(kernel):
-    """dram read+write bytes per launch recorded from an ncu capture of the
-    current kernel, if profiles/traffic.json holds one for it; else None."""
+def traffic_from_profiles(workload, kernel):
+    """dram read+write bytes per launch of `kernel` in `workload`, derived from
+    an ncu capture of the current kernel, if profiles/traffic.json holds one
+    ("workload:kernel" keys); else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        return d.get(kernel)
-    except (OSError, ValueError):
+        v = d.get(f"{workload}:{kernel}")
+        return v["bytes_per_launch"] if isinstance(v, dict) else v
+    except (OSError, ValueError, KeyError, TypeError):
         return None
 
 

@@ -818,8 +818,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
   if (pl.decode) return launch_decode(pl, A, M, K, Wq, Ws, N, C, st, wait_ns, status);
   if (pl.swap_ab) {
-    switch (pl.nx) {
-      case 16: return launch_cfg<kSwap, 16, 3>(a, grid, st);
+    switch (pl.nx) {   // M > 16 here: M <= 16 takes the decode kernel
       case 32: return launch_cfg<kSwap, 32, 4>(a, grid, st);
       case 64: return launch_cfg<kSwap, 64, 5>(a, grid, st);
       default: return launch_cfg<kSwap, 128, 4>(a, grid, st);

@@ -24,7 +24,7 @@ def _lib():
     a4w4.lib()
 
 
-@pytest.mark.parametrize("M,N,K", [(8, 7168, 4224), (300, 512, 4224)])
+@pytest.mark.parametrize("M,N,K", [(8, 7168, 4224), (300, 512, 4224), (1024, 5120, 1024)])
 def test_expired_wait_is_reported_and_context_survives(M, N, K):
     A_bits, W_bits = workloads.dense_problem(M, N, K, "decode")
     Wq = torch.empty(a4w4.a4w4_weight_codes_bytes(N, K), dtype=torch.uint8, device="cuda")
