@@ -541,15 +541,27 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           const int m = x_tile * 128 + lrow;
           const int n0 = w_tile * 256;
           if (p.splits == 1) {
-#pragma unroll 4
-            for (int c0 = 0; c0 < 256; c0 += 16) {
-              float v[16];
-              tmem_ld16(tq + c0, v);
-              if (m < p.M) {
-                uint4* dst = reinterpret_cast<uint4*>(p.C + static_cast<long long>(m) * p.N + n0 + c0);
-                dst[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-                dst[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]), pack_bf16x2(v[14], v[15]));
-              }
+            // Each thread stages its BF16 row in the drained ring (pitch 528
+            // bytes, so that a warp's row-parallel 16-byte stores spread over
+            // the banks) and writes it with one 512-byte bulk store, waiting
+            // until the store has read the row before the CTA may release the
+            // shared memory.
+            constexpr int kRowPitch = 528;
+            uint8_t* my = smem + lrow * kRowPitch;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 256; c0 += 64) {
+              float v[64];
+              tmem_ld64(tq + c0, v);
+              uint4* d = reinterpret_cast<uint4*>(my + c0 * 2);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+            }
+            fence_proxy_async_smem();
+            if (m < p.M) {
+              bulk_s2g(p.C + static_cast<long long>(m) * p.N + n0, base + static_cast<uint32_t>(lrow * kRowPitch), 512);
+              bulk_commit_wait_read();
             }
           } else if (p.cluster_reduce) {
             // fp32 partial [row][col] into this CTA's (drained) ring, rows padded
