@@ -204,9 +204,10 @@ class DenseSweep:
 
     def kernel_name(self, i):
         M, N, K = self.shapes[i]
-        if M <= 16:
-            kt = (K + 255) // 256
-            return f"a4w4_decode_kernel<16,{3 if (kt + 2) // 3 <= 8 else 4}>"
+        kt = (K + 255) // 256
+        if M <= 16 or (M <= 32 and kt <= 4):
+            ring = 3 if M <= 16 and (kt + 2) // 3 <= 8 else 4
+            return f"a4w4_decode_kernel<{16 if M <= 16 else 32},{ring}>"
         if 64 < M <= 128 and N // 256 >= 16:
             return "a4w4_gemm_kernel<normal,128>"
         if M <= 128:

@@ -1,5 +1,6 @@
-// decode.cu -- decode-size (M <= 16) dense A4W4 GEMM: weights stream at HBM
-// rate through the tcgen05 block-scaled MMA with the tokens on its N side.
+// decode.cu -- decode-size dense A4W4 GEMM (M <= 16; M <= 32 when one CTA
+// holds a whole K range): weights stream at HBM rate through the tcgen05
+// block-scaled MMA with the tokens on its N side.
 //
 // "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Summary/Implementation:
 // BF16 activations quantised inline to MXFP4 and multiplied with preshuffled
@@ -54,7 +55,7 @@ struct DecodeArgs {
 
 template <int NX, int SW, int SX>
 struct DCfg {
-  static constexpr int QWARPS = NX <= 32 ? 4 : 8;                // activation producer warps
+  static constexpr int QWARPS = NX <= 16 ? 4 : 8;                // activation producer warps
   static constexpr int THREADS = 64 + 32 * QWARPS;
   static constexpr int W_STAGE = 16384, WSF_STAGE = 1024;
   static constexpr int X_STAGE = NX * 128;
@@ -321,7 +322,12 @@ __global__ void __launch_bounds__(DCfg<NX, SW, SX>::THREADS, DCfg<NX, SW, SX>::M
       mbar_arrive(full_x);
     }
 
-    // ---------------- epilogue (warps 2..5, one per TMEM lane quadrant) ----------------
+    // ---------------- epilogue ----------------
+    // warps 2..5 (one per TMEM lane quadrant) drain the accumulator; with
+    // split-K every producer thread then takes part in the reduction, since
+    // the DSMEM stores of one thread complete one after another
+    volatile int* owner_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
+    float* red = reinterpret_cast<float*>(smem + Cf::OFF_W);   // partial [token][weight row], drained ring
     if (warp < 6) {
       named_bar_sync(2, 32 + 128);             // TMEM address published by the MMA warp
       tc_fence_after();
@@ -350,63 +356,62 @@ __global__ void __launch_bounds__(DCfg<NX, SW, SX>::THREADS, DCfg<NX, SW, SX>::M
             }
           }
         }
-      } else {
-        // park the partial [token][weight row] in the drained weight ring
-        float* red = reinterpret_cast<float*>(smem + Cf::OFF_W);
-        if (ready) {
+      } else if (ready) {
 #pragma unroll
-          for (int c0 = 0; c0 < NX; c0 += 16) {
-            if (c0 < mvalid) {
-              float v[16];
-              tmem_ld16(tq + c0, v);
+        for (int c0 = 0; c0 < NX; c0 += 16) {
+          if (c0 < mvalid) {
+            float v[16];
+            tmem_ld16(tq + c0, v);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + lrow] = v[j];
-            }
+            for (int j = 0; j < 16; ++j) red[(c0 + j) * 128 + lrow] = v[j];
           }
         }
-        named_bar_sync(1, 128);
-        cluster_wait();                          // every owner's mbarrier is initialised
-        cluster_waited = true;
-        const int S = p.splits;
-        const int et = threadIdx.x - 64;
-        const uint32_t rank = cluster_ctarank();
-        const int G = mvalid * 32;                   // float4 groups of the valid partial
-        const int slot = (G + S - 1) / S;
-        const float4* red4 = reinterpret_cast<const float4*>(red);
-        // group g belongs to owner o = max{o : floor(o*G/S) <= g}; sent whatever
-        // happened before, so that every owner's byte count completes
-        for (int g = et; g < G; g += 128) {
-          const int o = static_cast<int>((static_cast<long long>(g + 1) * S - 1) / G);
-          const int og0 = static_cast<int>(static_cast<long long>(o) * G / S);
-          const uint32_t dst = cluster_map_shared(
-              base + Cf::OFF_PUSH + static_cast<uint32_t>((static_cast<int>(rank) * slot + (g - og0)) * 16), static_cast<uint32_t>(o));
-          st_async_v4(dst, red4[g], cluster_map_shared(red_bar, static_cast<uint32_t>(o)));
-        }
-        // this CTA's slice: wait for all S x slice bytes (the limit exceeds any
-        // peer's bounded path to its stores), sum the slots in rank order
-        if (et == 0) {
-          const unsigned long long lim = 32ull * (p.wait_ns > drain_ns ? p.wait_ns : drain_ns);
-          *epi_ready = mbar_wait_cluster(red_bar, 0, lim, p.status) && ready ? 1 : 0;
-        }
-        named_bar_sync(1, 128);
-        if (*epi_ready) {
-          const int g0 = static_cast<int>(static_cast<long long>(rank) * G / S);
-          const int g1 = static_cast<int>(static_cast<long long>(rank + 1) * G / S);
-          const float4* push = reinterpret_cast<const float4*>(smem + Cf::OFF_PUSH);
-          for (int g = g0 + et; g < g1; g += 128) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c = 0; c < S; ++c) {
-              const float4 v = push[c * slot + (g - g0)];
-              acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
-            const int t = g >> 5, r4 = (g & 31) * 4;
-            uint2 o;
-            o.x = (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16) |
-                  __bfloat16_as_ushort(__float2bfloat16_rn(acc.x));
-            o.y = (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16) |
-                  __bfloat16_as_ushort(__float2bfloat16_rn(acc.z));
-            *reinterpret_cast<uint2*>(p.C + static_cast<long long>(m0 + t) * p.N + w_tile * 128 + r4) = o;
+      }
+    }
+    if (p.splits > 1) {
+      named_bar_sync(3, P);                    // partial staged, readiness published
+      const int ready = *epi_ready;
+      cluster_wait();                          // every owner's mbarrier is initialised
+      cluster_waited = true;
+      const int S = p.splits;
+      const int et = qt;
+      const uint32_t rank = cluster_ctarank();
+      const int G = mvalid * 32;                   // float4 groups of the valid partial
+      const int slot = (G + S - 1) / S;
+      const float4* red4 = reinterpret_cast<const float4*>(red);
+      // group g belongs to owner o = max{o : floor(o*G/S) <= g}; sent whatever
+      // happened before, so that every owner's byte count completes
+      for (int g = et; g < G; g += P) {
+        const int o = static_cast<int>((static_cast<long long>(g + 1) * S - 1) / G);
+        const int og0 = static_cast<int>(static_cast<long long>(o) * G / S);
+        const uint32_t dst = cluster_map_shared(
+            base + Cf::OFF_PUSH + static_cast<uint32_t>((static_cast<int>(rank) * slot + (g - og0)) * 16), static_cast<uint32_t>(o));
+        st_async_v4(dst, red4[g], cluster_map_shared(red_bar, static_cast<uint32_t>(o)));
+      }
+      // this CTA's slice: wait for all S x slice bytes (the limit exceeds any
+      // peer's bounded path to its stores), sum the slots in rank order
+      if (et == 0) {
+        const unsigned long long lim = 32ull * (p.wait_ns > drain_ns ? p.wait_ns : drain_ns);
+        *owner_ready = mbar_wait_cluster(red_bar, 0, lim, p.status) && ready ? 1 : 0;
+      }
+      named_bar_sync(3, P);
+      if (*owner_ready) {
+        const int g0 = static_cast<int>(static_cast<long long>(rank) * G / S);
+        const int g1 = static_cast<int>(static_cast<long long>(rank + 1) * G / S);
+        const float4* push = reinterpret_cast<const float4*>(smem + Cf::OFF_PUSH);
+        for (int g = g0 + et; g < g1; g += P) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < S; ++c) {
+            const float4 v = push[c * slot + (g - g0)];
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
           }
+          const int t = g >> 5, r4 = (g & 31) * 4;
+          uint2 o;
+          o.x = (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y))) << 16) |
+                __bfloat16_as_ushort(__float2bfloat16_rn(acc.x));
+          o.y = (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w))) << 16) |
+                __bfloat16_as_ushort(__float2bfloat16_rn(acc.z));
+          *reinterpret_cast<uint2*>(p.C + static_cast<long long>(m0 + t) * p.N + w_tile * 128 + r4) = o;
         }
       }
     }
@@ -468,9 +473,10 @@ int launch_decode(const GemmPlan& pl, const void* A, int M, int K, const void* W
   a.wait_ns = wait_ns;
   a.status = status;
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
-  switch (pl.ring) {
-    case 3: return launch_decode_cfg<16, 3, 3>(a, grid, st);
-    case 4: return launch_decode_cfg<16, 4, 4>(a, grid, st);
+  switch (pl.nx * 8 + pl.ring) {
+    case 16 * 8 + 3: return launch_decode_cfg<16, 3, 3>(a, grid, st);
+    case 16 * 8 + 4: return launch_decode_cfg<16, 4, 4>(a, grid, st);
+    case 32 * 8 + 4: return launch_decode_cfg<32, 4, 4>(a, grid, st);
     default: return -4;
   }
 }

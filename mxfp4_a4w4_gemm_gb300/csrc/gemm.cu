@@ -750,7 +750,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     pl.x_tiles = 1;
     ctas_per_sm = 1;
     tile_elems = static_cast<size_t>(128) * 256;
-  } else if (M <= 16) {
+  } else if (M <= 16 || (M <= 32 && pl.kt <= 4)) {
     // Decode kernel (decode.cu): the fewest K splits that let every CTA hold
     // its whole K range in its weight ring (all its weight copies in flight
     // at once), at most 8 (portable cluster size); no workspace.  A 3-deep
@@ -758,10 +758,14 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     // early and stream their weights); 4 deep when 3 would need over 8 splits.
     pl.swap_ab = 1;
     pl.decode = 1;
-    pl.nx = 16;
+    pl.nx = M <= 16 ? 16 : 32;
     pl.w_tiles = N / 128;
     pl.x_tiles = 1;
-    pl.ring = (pl.kt + 2) / 3 <= kMaxClusterSplits ? 3 : 4;
+    // 16 tokens: 3 CTAs fit per SM, so a 3-deep ring (more splits, more CTAs)
+    // still fits one wave; 32 tokens (taken here only when one CTA holds the
+    // whole K range: their 16 KB split-K partials reduce faster in the
+    // swap-AB kernel) fit 2 per SM, so the ring is 4 deep
+    pl.ring = (pl.nx == 16 && (pl.kt + 2) / 3 <= kMaxClusterSplits) ? 3 : 4;
     int splits = (pl.kt + pl.ring - 1) / pl.ring;
     if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
     if (splits < 1) splits = 1;
@@ -830,7 +834,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
   if (pl.decode) return launch_decode(pl, A, M, K, Wq, Ws, N, C, st, wait_ns, status);
   if (pl.swap_ab) {
-    switch (pl.nx) {   // M > 16 here: M <= 16 takes the decode kernel
+    switch (pl.nx) {
       case 32: return launch_cfg<kSwap, 32, 4>(a, grid, st);
       case 64: return launch_cfg<kSwap, 64, 5>(a, grid, st);
       default: return launch_cfg<kSwap, 128, 4>(a, grid, st);

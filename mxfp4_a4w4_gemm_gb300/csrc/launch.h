@@ -11,7 +11,7 @@ namespace a4w4 {
 // shared by a4w4_gemm and a4w4_gemm_workspace_bytes.
 struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
-  int decode;       // 1: M <= 16, the decode kernel (decode.cu)
+  int decode;       // 1: the decode kernel (decode.cu): M <= 16, or M <= 32 with K <= 1024
   int prequant;     // 1: activations quantised once into tiles first (large M)
   size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
@@ -42,7 +42,7 @@ int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_
 int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms);
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                 void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
-// M <= 16 (plan.decode): the decode kernel (decode.cu); no workspace.
+// plan.decode: the decode kernel (decode.cu); no workspace.
 int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                   void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
