@@ -209,7 +209,7 @@ class DenseSweep:
             ring = 3 if M <= 16 and (kt + 2) // 3 <= 8 else 4
             return f"a4w4_decode_kernel<{16 if M <= 16 else 32},{ring}>"
         if 64 < M <= 128 and N // 256 >= 16:
-            return "a4w4_gemm_kernel<normal,128>"
+            return "a4w4_gemm_kernel<prequant,128>"
         if M <= 128:
             nx = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
             return f"a4w4_gemm_kernel<swap,{nx}>"

@@ -670,18 +670,40 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       } else {
         const int m0 = x_tile * 128;
         const int rvalid = min(128, p.M - m0);
-        const int n = w_tile * 256 + 2 * et;
-        for (int r = static_cast<int>(rank); r < rvalid; r += S) {
-          const uint32_t off = red + static_cast<uint32_t>((r * kRedStride + 2 * et) * 4);
-          float ax = 0.f, ay = 0.f;
+        // this CTA owns rows rank, rank + S, ...: thread et sums 4 columns
+        // (16-byte remote loads) of every second of them, four rows in flight
+        // at once (remote loads are slow one at a time, fast together)
+        const int cq = et & 63, rsub = et >> 6;
+        const int n = w_tile * 256 + 4 * cq;
+        for (int j0 = 0;; j0 += 4) {
+          float4 acc[4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (c < S) {
-              const float2 v = ld_shared_cluster_f32x2(cluster_map_shared(off, c));
-              ax += v.x;
-              ay += v.y;
+          for (int u = 0; u < 4; ++u) {
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int r = static_cast<int>(rank) + S * (rsub + 2 * (j0 + u));
+            if (r < rvalid) {
+              const uint32_t off = red + static_cast<uint32_t>((r * kRedStride + 4 * cq) * 4);
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                if (c < S) {
+                  const float4 v = ld_shared_cluster_f32x4(cluster_map_shared(off, c));
+                  acc[u].x += v.x;
+                  acc[u].y += v.y;
+                  acc[u].z += v.z;
+                  acc[u].w += v.w;
+                }
             }
-          *reinterpret_cast<uint32_t*>(p.C + static_cast<long long>(m0 + r) * p.N + n) = pack_bf16x2(ax, ay);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = static_cast<int>(rank) + S * (rsub + 2 * (j0 + u));
+            if (r < rvalid)
+              *reinterpret_cast<uint2*>(p.C + static_cast<long long>(m0 + r) * p.N + n) =
+                  make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+          }
+          if (static_cast<int>(rank) + S * (rsub + 2 * (j0 + 4)) >= rvalid &&
+              static_cast<int>(rank) + S * (2 * (j0 + 4)) >= rvalid)
+            break;
         }
       }
     }
@@ -742,12 +764,16 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   int ctas_per_sm;
   size_t tile_elems;
   if (M > 64 && M <= 128 && N / 256 >= 16) {
-    // tokens on the MMA's 128-row side, weights on N = 256: fewer tensor-pipe
-    // instructions per weight byte than swap-AB once M passes 64
+    // tokens on the MMA's 128-row side, weights on N = 256: fewer operand
+    // bytes per weight byte than swap-AB once M passes 64.  The activations
+    // are quantised once into a tile (every weight tile's CTA would otherwise
+    // load the same BF16 rows, 4x the bytes of their MXFP4 codes).
     pl.swap_ab = 0;
+    pl.prequant = 1;
     pl.nx = 128;
     pl.w_tiles = N / 256;
     pl.x_tiles = 1;
+    pl.aq_bytes = static_cast<size_t>(pl.kt) * (16384 + 1024);
     ctas_per_sm = 1;
     tile_elems = static_cast<size_t>(128) * 256;
   } else if (M <= 16 || (M <= 32 && pl.kt <= 4)) {
