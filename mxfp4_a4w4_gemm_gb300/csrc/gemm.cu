@@ -28,7 +28,8 @@
 namespace a4w4 {
 
 // kSwap: weights x inline-quantised tokens (small M); kNormal: inline-quantised
-// rows x weights; kMoe: kNormal over gathered sorted rows with the SwiGLU +
+// rows x weights (the base of the MoE modes; dense GEMMs with M > 64 use kPre);
+// kMoe: kNormal over gathered sorted rows with the SwiGLU +
 // requant epilogue; kPre: rows quantised beforehand into tiles, both operands
 // streamed by TMA (large M); kMoePre: kMoe gathering rows that were quantised
 // once beforehand (plain MXFP4 layout) instead of quantising them per tile.
@@ -873,7 +874,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
     if (rc != 0) return rc;
     return launch_cfg<kPre, 128, 4>(a, grid, st);
   }
-  return launch_cfg<kNormal, 128, 4>(a, grid, st);
+  return -4;   // every plan is one of the above
 }
 
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
