@@ -14,6 +14,11 @@ namespace a4w4 {
 // Reads 64 bytes and writes 16 + 1 bytes per block: HBM-bound.
 __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const uint4* __restrict__ x, uint4* __restrict__ q,
                                                           uint8_t* __restrict__ s, long long nblocks) {
+  // programmatic dependent launch: x may come from the previous kernel; the
+  // next one (a GEMM that waits for this grid before reading q) may start its
+  // set-up now
+  griddep_wait();
+  griddep_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
     uint32_t w[16];
@@ -37,7 +42,13 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const uint4* __restric
 // 128*(n/256) + n%256 when n%256 < 128, else up row pair_I + 128*(n/256) + n%256 - 128.
 __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __restrict__ w, int rows, int valid_rows,
                                                              int K, int KT, int experts, int pair_I,
-                                                             uint8_t* __restrict__ wq, uint8_t* __restrict__ ws) {
+                                                             uint8_t* __restrict__ wq, uint8_t* __restrict__ ws,
+                                                             int early_trigger) {
+  griddep_wait();                // w may come from the previous kernel on the stream
+  // Activation tiles: the GEMM that follows waits for this grid before
+  // reading them, so it may start its set-up now.  Weights: the trigger stays
+  // at completion, since a GEMM with weight prefetch reads its weights early.
+  if (early_trigger) griddep_launch_dependents();
   const int kblocks = KT * 8;
   const long long total = static_cast<long long>(experts) * rows * kblocks;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -71,6 +82,25 @@ __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __r
   }
 }
 
+// Launch with programmatic stream serialisation (the kernels above order
+// their global reads after griddepcontrol.wait).  The one-time weight
+// preparation launches this way too but triggers its dependents only at
+// completion (see prepare_weight_kernel).
+template <typename... Params, typename... Args>
+static int launch_pdl(void (*kern)(Params...), int grid, int block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return -4;
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 static int grid_for(long long items, int threads, int sms, int per_sm) {
   long long g = (items + threads - 1) / threads;
   const long long cap = static_cast<long long>(sms) * per_sm;
@@ -81,28 +111,24 @@ static int grid_for(long long items, int threads, int sms, int per_sm) {
 
 int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms) {
   const long long nblocks = rows * (cols / 32);
-  mxfp4_quant_kernel<<<grid_for(nblocks, 256, sms, 8), 256, 0, st>>>(
-      static_cast<const uint4*>(x), static_cast<uint4*>(q), static_cast<uint8_t*>(s), nblocks);
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_pdl(mxfp4_quant_kernel, grid_for(nblocks, 256, sms, 8), 256, st, static_cast<const uint4*>(x),
+                    static_cast<uint4*>(q), static_cast<uint8_t*>(s), nblocks);
 }
 
 int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
                           cudaStream_t st, int sms) {
   const int KT = (K + 255) / 256;
   const long long items = static_cast<long long>(experts) * rows * KT * 8;
-  prepare_weight_kernel<<<grid_for(items, 256, sms, 8), 256, 0, st>>>(
-      static_cast<const uint16_t*>(w), rows, rows, K, KT, experts, pair_I, static_cast<uint8_t*>(wq),
-      static_cast<uint8_t*>(ws));
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_pdl(prepare_weight_kernel, grid_for(items, 256, sms, 8), 256, st, static_cast<const uint16_t*>(w),
+                    rows, rows, K, KT, experts, pair_I, static_cast<uint8_t*>(wq), static_cast<uint8_t*>(ws), 0);
 }
 
 int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms) {
   const int KT = (K + 255) / 256;
   const int rows = (M + 127) / 128 * 128;
   const long long items = static_cast<long long>(rows) * KT * 8;
-  prepare_weight_kernel<<<grid_for(items, 256, sms, 8), 256, 0, st>>>(
-      static_cast<const uint16_t*>(a), rows, M, K, KT, 1, 0, static_cast<uint8_t*>(aq), static_cast<uint8_t*>(as));
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+  return launch_pdl(prepare_weight_kernel, grid_for(items, 256, sms, 8), 256, st, static_cast<const uint16_t*>(a),
+                    rows, M, K, KT, 1, 0, static_cast<uint8_t*>(aq), static_cast<uint8_t*>(as), 1);
 }
 
 }  // namespace a4w4
