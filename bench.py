@@ -86,6 +86,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x, device):
+    """The largest of every rank's value of `x` (one all_reduce), or `x`
+    itself without a multi-rank process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, bytes_per_step, ms_per_step):
+    """Whole-job TB/s: every rank streams `bytes_per_step` per step (weak
+    scaling, independent replicas), timed by the slowest rank."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 
@@ -389,13 +407,9 @@ def run_ours(args, rank, world, local_rank):
             if time.time() - t_region > 0.5 or len(regions) >= 50:
                 break
         barrier()
-    region_ms = statistics.median(regions)
-    if world > 1:
-        t = torch.tensor([region_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(statistics.median(regions), dev)
     ms_per_step = region_ms / args.steps
-    value = world * wl.bytes_per_step / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, wl.bytes_per_step, ms_per_step)
 
     # per-GEMM launch durations: one graph per shape of `nrot` back-to-back
     # launches on rotating weight copies, timed with events on this stream
@@ -455,12 +469,8 @@ def run_ours(args, rank, world, local_rank):
         e2e_step(r)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * wl.bytes_per_step / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    e2e_value = job_throughput(world, wl.bytes_per_step, e2e_ms)
 
     status = a4w4.a4w4_get_device_status()
     if status != 0:
