@@ -224,7 +224,7 @@ class DenseSweep:
         M, N, K = self.shapes[i]
         kt = (K + 255) // 256
         if M <= 16 or (M <= 32 and kt <= 4):
-            ring = 3 if M <= 16 and (kt + 2) // 3 <= 8 else 4
+            ring = 3 if M <= 16 and (kt + 2) // 3 <= 16 else 4
             return f"a4w4_decode_kernel<{16 if M <= 16 else 32},{ring}>"
         if 64 < M <= 128 and N // 256 >= 16:
             return "a4w4_gemm_kernel<prequant,128>"

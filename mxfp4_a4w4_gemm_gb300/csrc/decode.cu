@@ -64,8 +64,9 @@ struct DCfg {
   static constexpr int OFF_X = OFF_W + SW * W_STAGE;
   static constexpr int OFF_WSF = OFF_X + SX * X_STAGE;
   static constexpr int OFF_XSF = OFF_WSF + SW * WSF_STAGE;
-  // push buffer: up to 8 rank slots of ceil(G / S) float4 groups, G = 32 x tokens
-  static constexpr int PUSH_BYTES = NX * 512 + 128;
+  // push buffer: up to 16 rank slots of ceil(G / S) float4 groups, G = 32 x tokens
+  // (S * ceil(G / S) <= G + S groups)
+  static constexpr int PUSH_BYTES = NX * 512 + 256;
   static constexpr int OFF_PUSH = OFF_XSF + SX * XSF_STAGE;
   static constexpr int OFF_BAR = OFF_PUSH + PUSH_BYTES;
   static constexpr int NBAR = 2 * SW + 4;
@@ -436,6 +437,9 @@ static int launch_decode_cfg(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
       return -4;
+    // clusters of up to 16 CTAs (more than the portable 8)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return -4;
     attr_done = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -463,6 +467,7 @@ static int launch_decode_cfg(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
 
 int launch_decode(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
                   cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
+  if (pl.splits < 1 || pl.splits > 16) return -4;   // push buffer and cluster limits
   DecodeArgs a{};
   a.A = static_cast<const uint16_t*>(A);
   a.Wq = static_cast<const uint8_t*>(Wq);

@@ -61,6 +61,7 @@ struct GemmArgs {
 
 constexpr int kRedStride = 260;      // floats per staged row of a 128x256 partial (1040 bytes)
 constexpr int kMaxClusterSplits = 8;  // portable cluster size
+constexpr int kMaxDecodeSplits = 16;  // decode kernel: non-portable clusters (a GPC holds at least 16 SMs)
 
 template <int MODE, int NX, int STAGES>
 struct Cfg {
@@ -780,7 +781,7 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   } else if (M <= 16 || (M <= 32 && pl.kt <= 4)) {
     // Decode kernel (decode.cu): the fewest K splits that let every CTA hold
     // its whole K range in its weight ring (all its weight copies in flight
-    // at once), at most 8 (portable cluster size); no workspace.  A 3-deep
+    // at once), at most 16 (a non-portable cluster size); no workspace.  A 3-deep
     // ring keeps three CTAs per SM (room for the next grid's CTAs to start
     // early and stream their weights); 4 deep when 3 would need over 8 splits.
     pl.swap_ab = 1;
@@ -792,9 +793,9 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     // still fits one wave; 32 tokens (taken here only when one CTA holds the
     // whole K range: their 16 KB split-K partials reduce faster in the
     // swap-AB kernel) fit 2 per SM, so the ring is 4 deep
-    pl.ring = (pl.nx == 16 && (pl.kt + 2) / 3 <= kMaxClusterSplits) ? 3 : 4;
+    pl.ring = (pl.nx == 16 && (pl.kt + 2) / 3 <= kMaxDecodeSplits) ? 3 : 4;
     int splits = (pl.kt + pl.ring - 1) / pl.ring;
-    if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
+    if (splits > kMaxDecodeSplits) splits = kMaxDecodeSplits;
     if (splits < 1) splits = 1;
     pl.splits = splits;
     pl.cluster_reduce = splits > 1;

@@ -74,7 +74,8 @@ def test_ragged_m_spans_tiles(M):
 @pytest.mark.parametrize("M,N,K", [(8, 256, 128), (8, 256, 384), (200, 768, 4224), (40, 1536, 4224),
                                    (3, 2048, 2304), (130, 256, 256),
                                    # K ranges longer than a CTA's operand rings (several fill/drain rounds)
-                                   (1, 256, 16384), (24, 512, 12288), (50, 256, 10368),
+                                   (1, 256, 16384), (1, 256, 20480), (9, 256, 17408), (24, 512, 12288),
+                                   (50, 256, 10368),
                                    # large-M tiles without split-K: one K tile; K range longer than the ring
                                    (256, 512, 256), (1024, 5120, 1536)])
 def test_k_tails_and_shapes(M, N, K):
