@@ -760,6 +760,22 @@ static int launch_cfg(const GemmArgs& a, dim3 grid, cudaStream_t st) {
 
 static int swap_nx(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
 
+// Decode kernel: K splits per 128-row weight tile.  The fewest that let each
+// CTA hold its whole K range in its `ring`-deep weight ring (every weight copy
+// in flight at once); once split-K is needed at all, raised until the grid
+// fills two CTAs per SM (more weight streams in flight), keeping at least one
+// K tile per CTA and at most 16 CTAs per cluster (non-portable size).
+static int decode_splits(int kt, int ring, int w_tiles, int sms) {
+  int splits = (kt + ring - 1) / ring;
+  if (splits > 1) {
+    int fill = 2 * sms / (w_tiles > 0 ? w_tiles : 1);
+    if (fill > kt) fill = kt;
+    if (fill > splits) splits = fill;
+  }
+  if (splits > kMaxDecodeSplits) splits = kMaxDecodeSplits;
+  return splits < 1 ? 1 : splits;
+}
+
 GemmPlan plan_gemm(int M, int N, int K, int sms) {
   GemmPlan pl{};
   pl.kt = (K + 255) / 256;
@@ -778,27 +794,22 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     pl.aq_bytes = static_cast<size_t>(pl.kt) * (16384 + 1024);
     ctas_per_sm = 1;
     tile_elems = static_cast<size_t>(128) * 256;
-  } else if (M <= 16 || (M <= 32 && pl.kt <= 4)) {
-    // Decode kernel (decode.cu): the fewest K splits that let every CTA hold
-    // its whole K range in its weight ring (all its weight copies in flight
-    // at once), at most 16 (a non-portable cluster size); no workspace.  A 3-deep
-    // ring keeps three CTAs per SM (room for the next grid's CTAs to start
-    // early and stream their weights); 4 deep when 3 would need over 8 splits.
+  } else if (M <= 16 || (M <= 32 && (pl.kt <= 4 || decode_splits(pl.kt, 4, N / 128, sms) > kMaxClusterSplits))) {
+    // Decode kernel (decode.cu), no workspace.  16 tokens: 3 CTAs fit per SM,
+    // so a 3-deep ring (room for the next grid's CTAs to start early and
+    // stream their weights), 4 deep when 3 would need over 16 splits.  32
+    // tokens fit 2 per SM (4-deep ring); the swap-AB kernel reduces their
+    // 16 KB split-K partials as fast, so they come here only when one CTA
+    // holds the whole K range or when 16-wide clusters give the grid more
+    // CTAs than its 8-wide ones.
     pl.swap_ab = 1;
     pl.decode = 1;
     pl.nx = M <= 16 ? 16 : 32;
     pl.w_tiles = N / 128;
     pl.x_tiles = 1;
-    // 16 tokens: 3 CTAs fit per SM, so a 3-deep ring (more splits, more CTAs)
-    // still fits one wave; 32 tokens (taken here only when one CTA holds the
-    // whole K range: their 16 KB split-K partials reduce faster in the
-    // swap-AB kernel) fit 2 per SM, so the ring is 4 deep
     pl.ring = (pl.nx == 16 && (pl.kt + 2) / 3 <= kMaxDecodeSplits) ? 3 : 4;
-    int splits = (pl.kt + pl.ring - 1) / pl.ring;
-    if (splits > kMaxDecodeSplits) splits = kMaxDecodeSplits;
-    if (splits < 1) splits = 1;
-    pl.splits = splits;
-    pl.cluster_reduce = splits > 1;
+    pl.splits = decode_splits(pl.kt, pl.ring, pl.w_tiles, sms);
+    pl.cluster_reduce = pl.splits > 1;
     return pl;
   } else if (M <= 128) {
     pl.swap_ab = 1;

@@ -76,6 +76,8 @@ def test_ragged_m_spans_tiles(M):
                                    # K ranges longer than a CTA's operand rings (several fill/drain rounds)
                                    (1, 256, 16384), (1, 256, 20480), (9, 256, 17408), (24, 512, 12288),
                                    (50, 256, 10368),
+                                   # decode kernel with 16 K splits filling the grid (uneven K ranges)
+                                   (16, 1536, 7168), (17, 1536, 4224), (32, 512, 7168),
                                    # large-M tiles without split-K: one K tile; K range longer than the ring
                                    (256, 512, 256), (1024, 5120, 1536)])
 def test_k_tails_and_shapes(M, N, K):
