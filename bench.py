@@ -187,15 +187,34 @@ class DenseSweep:
             self.wq[(N, K)] = [q] + [q.clone() for _ in range(self.copies - 1)]
             self.ws[(N, K)] = [s] + [s.clone() for _ in range(self.copies - 1)]
             del W
-        self.A, self.C, self.A_host, self.C_host = [], [], [], []
+        # A step's activations (and outputs) are views into one device buffer
+        # with one pinned host mirror, so the end-to-end step moves them with
+        # one copy each way (every view starts on a 256-byte boundary: K % 128 == 0,
+        # N % 256 == 0).  Two such I/O slots let one step's copies overlap
+        # another step's kernels; `slot` selects the one that calls use.
+        a_elems = sum(M * K for M, _, K in self.shapes)
+        c_elems = sum(M * N for M, N, _ in self.shapes)
+        a_host = torch.empty(a_elems, dtype=torch.bfloat16)
+        ao = 0
         for M, N, K in self.shapes:
             A_bits, _ = workloads.dense_problem(M, N, K, family) if family != "decode" else (
                 workloads.decode_activation_bits(M, K), None)
-            a = workloads.bits_to_torch(A_bits)
-            self.A_host.append(a.pin_memory())
-            self.A.append(a.to(dev))
-            self.C.append(torch.empty((M, N), dtype=torch.bfloat16, device=dev))
-            self.C_host.append(torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+            a_host[ao:ao + M * K].copy_(workloads.bits_to_torch(A_bits).reshape(-1))
+            ao += M * K
+        self.slot = 0
+        self.A_host = [a_host.pin_memory() for _ in range(2)]
+        self.C_host = [torch.empty(c_elems, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        self.A_dev = [torch.empty(a_elems, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.C_dev = [torch.empty(c_elems, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.A, self.C = [[], []], [[], []]
+        for b in range(2):
+            ao = co = 0
+            for M, N, K in self.shapes:
+                self.A[b].append(self.A_dev[b][ao:ao + M * K].view(M, K))
+                self.C[b].append(self.C_dev[b][co:co + M * N].view(M, N))
+                ao += M * K
+                co += M * N
+            self.A_dev[b].copy_(self.A_host[b])
         self.ws_bytes = max(a4w4.a4w4_gemm_workspace_bytes(M, N, K) for M, N, K in self.shapes)
         self.work = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
         a4w4.a4w4_workspace_init(self.work, self.ws_bytes)
@@ -207,20 +226,18 @@ class DenseSweep:
     def call(self, i, r):
         M, N, K = self.shapes[i]
         c = (r * len(self.shapes) + i) % self.copies
-        self.a4w4.a4w4_gemm(self.A[i], M, K, self.wq[(N, K)][c], self.ws[(N, K)][c], N, self.C[i],
-                            self.work, self.ws_bytes)
+        self.a4w4.a4w4_gemm(self.A[self.slot][i], M, K, self.wq[(N, K)][c], self.ws[(N, K)][c], N,
+                            self.C[self.slot][i], self.work, self.ws_bytes)
 
     def step(self, r):
         for i in range(len(self.shapes)):
             self.call(i, r)
 
-    def h2d(self):
-        for a_d, a_h in zip(self.A, self.A_host):
-            a_d.copy_(a_h, non_blocking=True)
+    def h2d(self, b):
+        self.A_dev[b].copy_(self.A_host[b], non_blocking=True)
 
-    def d2h(self):
-        for c_h, c_d in zip(self.C_host, self.C):
-            c_h.copy_(c_d, non_blocking=True)
+    def d2h(self, b):
+        self.C_host[b].copy_(self.C_dev[b], non_blocking=True)
 
     @property
     def h2d_bytes(self):
@@ -283,13 +300,18 @@ class MoeSweep:
                     ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
             # quantise tokens once (workspace) unless T = 1 or inline quant is forced
             xwsb = 0 if (T == 1 or self.inline) else a4w4.a4w4_moe_gemm1_workspace_bytes(T, self.D)
+            # tokens and outputs in two I/O slots (see DenseSweep); sort and
+            # quantisation workspaces are used by the kernels alone
+            R = T * self.topk
             self.items.append(dict(
-                T=T, X=X.to(dev), X_host=X.pin_memory(), routes=routes, xwsb=xwsb,
+                T=T, X=[X.to(dev) for _ in range(2)], X_host=[X.pin_memory() for _ in range(2)],
+                routes=routes, xwsb=xwsb,
                 xws=torch.empty(max(xwsb, 16), dtype=torch.uint8, device=dev) if xwsb else None,
-                q=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8, device=dev),
-                s=torch.empty((T * self.topk, self.I // 32), dtype=torch.uint8, device=dev),
-                q_host=torch.empty((T * self.topk, self.I // 2), dtype=torch.uint8).pin_memory(),
-                s_host=torch.empty((T * self.topk, self.I // 32), dtype=torch.uint8).pin_memory()))
+                q=[torch.empty((R, self.I // 2), dtype=torch.uint8, device=dev) for _ in range(2)],
+                s=[torch.empty((R, self.I // 32), dtype=torch.uint8, device=dev) for _ in range(2)],
+                q_host=[torch.empty((R, self.I // 2), dtype=torch.uint8).pin_memory() for _ in range(2)],
+                s_host=[torch.empty((R, self.I // 32), dtype=torch.uint8).pin_memory() for _ in range(2)]))
+        self.slot = 0
         self.shapes = [(it["T"], 2 * self.I, self.D) for it in self.items]
         self.launches_per_step = 4 * len(self.items)      # 3 sort kernels + GEMM1 per T
         self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
@@ -309,21 +331,23 @@ class MoeSweep:
             self.a4w4.a4w4_moe_sort(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
                                     ro["ws"], ro["wsb"])
         if gemm:
-            self.a4w4.a4w4_moe_gemm1(it["X"], T, self.D, ro["rows"], ro["bexp"], ro["nb"], self.topk, self.W1q,
-                                     self.W1s, self.E, self.I, it["q"], it["s"], it["xws"], it["xwsb"])
+            b = self.slot
+            self.a4w4.a4w4_moe_gemm1(it["X"][b], T, self.D, ro["rows"], ro["bexp"], ro["nb"], self.topk,
+                                     self.W1q, self.W1s, self.E, self.I, it["q"][b], it["s"][b], it["xws"],
+                                     it["xwsb"])
 
     def step(self, r):
         for i in range(len(self.items)):
             self.call(i, r)
 
-    def h2d(self):
+    def h2d(self, b):
         for it in self.items:
-            it["X"].copy_(it["X_host"], non_blocking=True)
+            it["X"][b].copy_(it["X_host"][b], non_blocking=True)
 
-    def d2h(self):
+    def d2h(self, b):
         for it in self.items:
-            it["q_host"].copy_(it["q"], non_blocking=True)
-            it["s_host"].copy_(it["s"], non_blocking=True)
+            it["q_host"][b].copy_(it["q"][b], non_blocking=True)
+            it["s_host"][b].copy_(it["s"][b], non_blocking=True)
 
     @property
     def h2d_bytes(self):
@@ -465,19 +489,58 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic_from_profiles(args.workload, dom), "peak_source": f"{peak_src} hbm_gbs",
                 "bytes_per_launch": round(dom_bytes / dom_n), "avg_launch_us": round(dom_us / dom_n, 3)}
 
-    # end to end through the C ABI with host buffers
+    # End to end through the C ABI with host buffers, pipelined as a serving
+    # loop would run it: step r's inputs go up on one copy stream and its
+    # outputs come back on another, in I/O slot r % 2, so step r+1's upload
+    # and step r-1's download overlap step r's kernels.  A slot is refilled
+    # only after the kernels of step r-2 stopped reading it and its outputs
+    # were read back; every step's copies lie inside the timed region.
+    e2e_graphs = []
+    for r in range(2 * nrot):
+        wl.slot = r % 2
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            wl.step(r)
+        e2e_graphs.append(g)
+    wl.slot = 0
+    torch.cuda.synchronize()
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    up = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    down = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
     def e2e_step(r):
-        wl.h2d()
-        step_graphs[r % nrot].replay()
-        wl.d2h()
-    for r in range(3):
+        b = r % 2
+        with torch.cuda.stream(s_up):
+            if used[b]:
+                s_up.wait_event(done[b])
+            wl.h2d(b)
+            up[b].record(s_up)
+        stream.wait_event(up[b])
+        if used[b]:
+            stream.wait_event(down[b])
+        e2e_graphs[r % len(e2e_graphs)].replay()
+        done[b].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(done[b])
+            wl.d2h(b)
+            down[b].record(s_down)
+        used[b] = True
+
+    for r in range(4):
         e2e_step(r)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_up.wait_event(e0)
+    s_down.wait_event(e0)
     for r in range(args.steps):
         e2e_step(r)
+    for b in range(2):
+        if used[b]:
+            stream.wait_event(down[b])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
@@ -505,6 +568,7 @@ def run_ours(args, rank, world, local_rank):
                    "per_gemm": per, "timed_regions": len(regions)},
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 4), "unit": "TB/s", "ms_per_step": round(e2e_ms, 5),
+                "pipeline": "pinned host buffers, two I/O slots; H2D, kernels and D2H on three streams",
                 "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
         "gpu_launches": args.steps * wl.launches_per_step * len(regions),
         "clocks": clk.summary(),
