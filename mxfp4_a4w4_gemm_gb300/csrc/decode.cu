@@ -433,15 +433,14 @@ template <int NX, int SW, int SX>
 static int launch_decode_cfg(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
   using Cf = DCfg<NX, SW, SX>;
   auto kern = a4w4_decode_kernel<NX, SW, SX>;
-  static bool attr_done = false;   // per instantiation; benign race (idempotent)
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
-      return -4;
-    // clusters of up to 16 CTAs (more than the portable 8)
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return -4;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_devs{0};   // bit d: attributes set on device d
+  if (ensure_func_attrs(attr_devs, [&] {
+        // clusters of up to 16 CTAs (more than the portable 8)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+      }) != 0)
+    return -4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(Cf::THREADS, 1, 1);

@@ -729,12 +729,11 @@ template <int MODE, int NX, int STAGES>
 static int launch_cfg(const GemmArgs& a, dim3 grid, cudaStream_t st) {
   using Cf = Cfg<MODE, NX, STAGES>;
   auto kern = a4w4_gemm_kernel<MODE, NX, STAGES>;
-  static bool attr_done = false;   // per instantiation; benign race (idempotent)
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) != cudaSuccess)
-      return -4;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_devs{0};   // bit d: attributes set on device d
+  if (ensure_func_attrs(attr_devs, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES) == cudaSuccess;
+      }) != 0)
+    return -4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(Cf::THREADS, 1, 1);

@@ -1,6 +1,7 @@
 // launch.h -- host-side launchers behind the C ABI (internal).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -11,7 +12,7 @@ namespace a4w4 {
 // shared by a4w4_gemm and a4w4_gemm_workspace_bytes.
 struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
-  int decode;       // 1: the decode kernel (decode.cu): M <= 16, or M <= 32 with K <= 1024
+  int decode;       // 1: the decode kernel (decode.cu): M <= 16, and some M <= 32 (plan_gemm)
   int prequant;     // 1: activations quantised once into tiles first (large M)
   size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
@@ -26,6 +27,22 @@ struct GemmPlan {
 };
 
 GemmPlan plan_gemm(int M, int N, int K, int sms);
+
+// Kernel function attributes (dynamic shared memory size, non-portable
+// cluster sizes) belong to the current device's context.  A launcher keeps
+// one bit per device in `done` and runs `set` only where that bit is clear
+// (devices beyond 63 run it on every launch).  Returns 0, or -4 when the
+// device cannot be read or `set` reports a failed attribute call.
+template <typename SetFn>
+int ensure_func_attrs(std::atomic<unsigned long long>& done, SetFn set) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -4;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return 0;
+  if (!set()) return -4;
+  if (bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return 0;
+}
 
 // Shared by the C ABI entry points (defined in api.cu): SM count of the
 // current device if it is a compute capability 10.3 GPU, else a negative
