@@ -80,8 +80,11 @@ int a4w4_prepare_gemm_weight(const void* W_bf16, int N, int K, void* Wq, void* W
  *   A_bf16 [M, K] row-major; Wq, Ws from a4w4_prepare_gemm_weight(N, K);
  *   C_bf16 [M, N] row-major, rows >= M are never touched.
  *   M >= 1, N % 256 == 0, K % 128 == 0.
- * Small M uses weights-as-rows tiles (swap-AB) with split-K over the SMs;
- * split-K needs `workspace` (fp32 partial tiles + tile counters) of at least
+ * Small M uses weights-as-rows tiles (swap-AB) with split-K over the SMs,
+ * reduced inside thread-block clusters (no workspace).  `workspace` holds,
+ * where the plan needs them, the activations quantised once into tiles
+ * (M > 64) and fp32 split-K partial tiles + tile counters (a tile split over
+ * more CTAs than one cluster holds).  It must be at least
  * a4w4_gemm_workspace_bytes(M, N, K) bytes, zeroed once by a4w4_workspace_init
  * (the counters reset themselves after each call; re-initialise after a
  * TIMEOUT).  When that size is 0 the workspace may be NULL.  The reduction
