@@ -84,11 +84,10 @@ int a4w4_prepare_gemm_weight(const void* W_bf16, int N, int K, void* Wq, void* W
  * reduced inside thread-block clusters (no workspace).  `workspace` holds,
  * where the plan needs them, the activations quantised once into tiles
  * (M > 128; M > 64 when N >= 4096) and fp32 split-K partial tiles + tile
- * counters (a tile split over more CTAs than one cluster holds).  It must be
- * at least
- * a4w4_gemm_workspace_bytes(M, N, K) bytes, zeroed once by a4w4_workspace_init
- * (the counters reset themselves after each call; re-initialise after a
- * TIMEOUT).  When that size is 0 the workspace may be NULL.  The reduction
+ * counters (a tile split over more CTAs than one cluster holds).  It must
+ * hold at least a4w4_gemm_workspace_bytes(M, N, K) bytes, zeroed once by
+ * a4w4_workspace_init (the counters reset themselves after each call;
+ * re-initialise after a TIMEOUT).  When that size is 0 the workspace may be NULL.  The reduction
  * order is fixed, so results are bitwise deterministic. */
 size_t a4w4_gemm_workspace_bytes(int M, int N, int K);
 int a4w4_workspace_init(void* workspace, size_t ws_bytes, void* stream);
