@@ -158,16 +158,6 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # dense workloads on the GPU
 
-def decode_splits(kt, ring, w_tiles, sms):
-    """The library's K-split rule for the decode kernel (names the launched
-    instantiation): the fewest splits whose CTAs hold their K range in the
-    ring, raised to fill two CTAs per SM once split-K is needed, <= kt, <= 16."""
-    splits = -(-kt // ring)
-    if splits > 1:
-        splits = max(splits, min(kt, 2 * sms // max(w_tiles, 1)))
-    return max(1, min(splits, 16))
-
-
 class DenseSweep:
     def __init__(self, shapes, family, dev):
         import torch
@@ -249,17 +239,7 @@ class DenseSweep:
 
     def kernel_name(self, i):
         M, N, K = self.shapes[i]
-        kt = (K + 255) // 256
-        sms = self.torch.cuda.get_device_properties(self.dev).multi_processor_count
-        if M <= 16 or (M <= 32 and (kt <= 4 or decode_splits(kt, 4, N // 128, sms) > 8)):
-            ring = 3 if M <= 16 and (kt + 2) // 3 <= 16 else 4
-            return f"a4w4_decode_kernel<{16 if M <= 16 else 32},{ring}>"
-        if 64 < M <= 128 and N // 256 >= 16:
-            return "a4w4_gemm_kernel<prequant,128>"
-        if M <= 128:
-            nx = 16 if M <= 16 else 32 if M <= 32 else 64 if M <= 64 else 128
-            return f"a4w4_gemm_kernel<swap,{nx}>"
-        return "a4w4_gemm_kernel<prequant,128>"
+        return self.a4w4.a4w4_gemm_kernel_name(M, N, K)   # the library's own plan
 
     def label(self, i):
         M, N, K = self.shapes[i]

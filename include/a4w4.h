@@ -91,6 +91,15 @@ int a4w4_prepare_gemm_weight(const void* W_bf16, int N, int K, void* Wq, void* W
  * order is fixed, so results are bitwise deterministic. */
 size_t a4w4_gemm_workspace_bytes(int M, int N, int K);
 int a4w4_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+/* Name of the kernel instantiation a4w4_gemm(M, N, K) launches on the current
+ * device (planned for GB300's 152 SMs when no device is visible), e.g.
+ * "a4w4_decode_kernel<16,3>" (tokens per CTA, weight ring depth) or
+ * "a4w4_gemm_kernel<swap,32>" / "a4w4_gemm_kernel<prequant,128>"; the
+ * quantise-once plans also launch the activation pre-pass.  Host-only, no
+ * device work.  Writes a NUL-terminated string of at most n bytes (truncated)
+ * into buf.  Returns A4W4_OK, or A4W4_ERR_ARG for a shape a4w4_gemm rejects,
+ * a NULL buf or n == 0. */
+int a4w4_gemm_kernel_name(int M, int N, int K, char* buf, size_t n);
 int a4w4_gemm(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
               void* C_bf16, void* workspace, size_t ws_bytes, void* stream);
 

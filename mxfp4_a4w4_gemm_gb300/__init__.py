@@ -12,6 +12,7 @@ from ._native import (  # noqa: F401
     LIB_PATH,
     SIGNATURES,
     a4w4_gemm,
+    a4w4_gemm_kernel_name,
     a4w4_gemm_noalloc,
     a4w4_gemm_workspace_bytes,
     a4w4_get_device_status,

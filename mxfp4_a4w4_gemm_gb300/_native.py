@@ -22,6 +22,7 @@ SIGNATURES = {
     "a4w4_weight_scales_bytes": (_c_size, [_c_int, _c_int]),
     "a4w4_prepare_gemm_weight": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
     "a4w4_gemm_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_gemm_kernel_name": (_c_int, [_c_int, _c_int, _c_int, ctypes.c_char_p, _c_size]),
     "a4w4_workspace_init": (_c_int, [_vp, _c_size, _vp]),
     "a4w4_gemm": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, _vp]),
     "a4w4_mxfp4_quant": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
@@ -111,6 +112,12 @@ def a4w4_prepare_gemm_weight(W, N, K, Wq, Ws, stream=None):
 
 def a4w4_gemm_workspace_bytes(M, N, K):
     return lib().a4w4_gemm_workspace_bytes(M, N, K)
+
+
+def a4w4_gemm_kernel_name(M, N, K):
+    buf = ctypes.create_string_buffer(96)
+    _check("a4w4_gemm_kernel_name", lib().a4w4_gemm_kernel_name(M, N, K, buf, len(buf)))
+    return buf.value.decode()
 
 
 def a4w4_workspace_init(workspace, ws_bytes, stream=None):

@@ -2,6 +2,7 @@
 // argument validation, device checks, launch, and the device status word.
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 
 #include "a4w4.h"
 #include "launch.h"
@@ -101,6 +102,18 @@ int a4w4_prepare_gemm_weight(const void* W_bf16, int N, int K, void* Wq, void* W
 size_t a4w4_gemm_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   return a4w4::plan_gemm(M, N, K, sizing_sms()).ws_bytes;
+}
+
+int a4w4_gemm_kernel_name(int M, int N, int K, char* buf, size_t n) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0 || buf == nullptr || n == 0) return A4W4_ERR_ARG;
+  const a4w4::GemmPlan pl = a4w4::plan_gemm(M, N, K, sizing_sms());
+  if (pl.decode)
+    snprintf(buf, n, "a4w4_decode_kernel<%d,%d>", pl.nx, pl.ring);
+  else if (pl.prequant)
+    snprintf(buf, n, "a4w4_gemm_kernel<prequant,%d>", pl.nx);
+  else
+    snprintf(buf, n, "a4w4_gemm_kernel<swap,%d>", pl.nx);
+  return A4W4_OK;
 }
 
 int a4w4_workspace_init(void* workspace, size_t ws_bytes, void* stream) {

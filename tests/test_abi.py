@@ -45,6 +45,26 @@ def test_size_functions():
     assert a4w4.a4w4_gemm_workspace_bytes(1, 1536, 7168) == 0
 
 
+def test_kernel_routing_of_the_workload_shapes():
+    # planned for GB300's 152 SMs when no device is visible (as on the GPU)
+    name = a4w4.a4w4_gemm_kernel_name
+    for K in (4224, 7168, 768):
+        N = 1536 if K == 7168 else 7168
+        for M in (1, 8):
+            assert name(M, N, K) == "a4w4_decode_kernel<16,3>"
+    assert name(32, 7168, 4224) == "a4w4_gemm_kernel<swap,32>"      # 5 splits: swap-AB's clusters suffice
+    assert name(32, 1536, 7168) == "a4w4_decode_kernel<32,4>"       # 16 splits fill the grid
+    assert name(32, 7168, 768) == "a4w4_decode_kernel<32,4>"        # one CTA holds the K range
+    assert name(1, 256, 16384 * 4) == "a4w4_decode_kernel<16,4>"    # a 3-deep ring would need > 16 splits
+    assert name(37, 1536, 4224) == "a4w4_gemm_kernel<swap,64>"
+    assert name(100, 1536, 4224) == "a4w4_gemm_kernel<swap,128>"     # N < 4096: swap-AB up to 128 tokens
+    for M in (128, 512, 2048):
+        assert name(M, 8448, 7168) == "a4w4_gemm_kernel<prequant,128>"
+    with pytest.raises(a4w4.A4W4Error) as e:
+        name(1, 300, 256)
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+
+
 def test_argument_errors_need_no_device():
     with pytest.raises(a4w4.A4W4Error) as e:
         a4w4.a4w4_gemm(16, 1, 256, 16, 16, 300, 16, stream=0)        # N % 256 != 0
