@@ -1,14 +1,25 @@
 """Benchmark of the MXFP4 A4W4 GEMM path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|small|large|stress|moe]
+                    [--workload all|decode|small|large|stress|moe]
 
-Prints ONE JSON line (rank 0).  A step is one pass of the path over the
-workload: for the default ``decode`` workload, the nine decode-size GEMMs
-M in {1, 8, 32} x (N, K) in {(7168, 4224), (1536, 7168), (7168, 768)} (BF16
-activations N(0,1) with 1% x20 outlier channels, MXFP4 weights from N(0,0.02)),
-each one launch of the fused quant + tcgen05 block-scaled GEMM + BF16
-epilogue.  Weights are prepared once, outside timing, as on the source page.
+Prints ONE JSON line (rank 0).  The default (``all``) measures every workload
+of the metric "M = 1-2048" in one invocation:
+
+* ``decode`` (the headline: ``value``, ``roofline``, ``e2e``, ``cpu_baseline``)
+  -- the nine decode-size GEMMs M in {1, 8, 32} x (N, K) in {(7168, 4224),
+  (1536, 7168), (7168, 768)}, BF16 activations N(0,1) with 1% x20 outlier
+  channels, MXFP4 weights from N(0,0.02);
+* ``large`` -- M in {128, 512, 2048} x (N, K) in {(8448, 7168), (7168, 4224)};
+* ``stress`` -- M in {37, 513, 2047}, N = 1536, K = 4224, scale-edge blocks;
+* ``moe`` -- grouped MoE GEMM1 + SwiGLU + MXFP4 requant, T in {1, 16, 256,
+  4096}, E = 896, topk = 16, D = 3584, I = 768 (sort + GEMM1 per T);
+
+each under ``configs`` with its own step time, per-GEMM table, roofline,
+end-to-end figures, clocks and CPU-oracle baseline.  A step is one pass over
+the workload's GEMMs, each one launch of the fused quant + tcgen05
+block-scaled GEMM + epilogue (the quantise-once plans add the activation
+pre-pass).  Weights are prepared once, outside timing, as on the source page.
 
 Timing: W warm-up steps, then K steps replayed from CUDA graphs, bracketed by
 a barrier and torch.cuda.synchronize(), CUDA events on the launching stream.
@@ -19,18 +30,21 @@ value  = sum of algorithmic bytes (N*K/2 + N*K/32 + 2*M*K + 2*M*N per GEMM)
          over the step / step time, in TB/s (whole job: all ranks' bytes over
          the slowest rank's time).
 e2e    = the same metric with each step's activations copied from pinned host
-         memory and its outputs copied back inside the timed region.
+         memory and its outputs copied back inside the timed region (graphs of
+         the C ABI calls; ``e2e_eager`` issues every C ABI call from Python
+         instead, so the host cost of the calls is inside the time too).
 N > 1: replicas only (the GEMMs of different ranks are independent; no
 collective on the data path).
 
 ``--impl reference`` times the CPU oracle (oracle/) on a bounded sample of the
-same workload on the host cores and prints the same line with "impl":
+headline workload on the host cores and prints the same line with "impl":
 "reference".
 """
 
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -48,11 +62,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP4_OVER_BF16 = 13.5 / 2.25       # nominal dense ratio (fp4 13.5 PF, bf16 2.25 PF per GPU)
 L2_BYTES = 126 * 1024 * 1024
 
-# Source page's microbenchmark (MI355X, median us) for the decode-size points:
-# "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Kernel microbenchmark.
+# Source page's microbenchmark (MI355X, median us; another machine: context,
+# not a baseline): "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM",
+# Kernel microbenchmark.
 PAGES_US = {(7168, 4224, 1): 15.960, (7168, 4224, 8): 23.041, (7168, 4224, 32): 23.520,
             (1536, 7168, 1): 18.420, (1536, 7168, 8): 23.320, (1536, 7168, 32): 26.181,
-            (7168, 768, 1): 12.580, (7168, 768, 8): 11.921, (7168, 768, 32): 12.120}
+            (7168, 768, 1): 12.580, (7168, 768, 8): 11.921, (7168, 768, 32): 12.120,
+            (8448, 7168, 128): 60.121, (8448, 7168, 512): 89.480, (8448, 7168, 2048): 237.863,
+            (7168, 4224, 128): 23.280, (7168, 4224, 512): 50.041, (7168, 4224, 2048): 107.041}
+# "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Performance (gfx1250, fused
+# GEMM1 operator latency in us by token count; SiTUv2 there, SwiGLU here)
+PAGES_MOE_US = {1: 47.39, 16: 201.41, 256: 676.86, 4096: 1351.28}
+ALL_WORKLOADS = ["decode", "large", "stress", "moe"]
 
 WORKLOADS = {
     "decode": ("decode-size dense A4W4 sweep, M in {1,8,32} x (N,K) in {(7168,4224),(1536,7168),(7168,768)}",
@@ -210,14 +231,16 @@ class DenseSweep:
         a4w4.a4w4_workspace_init(self.work, self.ws_bytes)
         self.bytes_per_step = sum(gemm_bytes(*s) for s in self.shapes)
         self.flops_per_step = sum(gemm_flops(*s) for s in self.shapes)
-        self.launches_per_step = len(self.shapes)
+        # the quantise-once plans launch the activation pre-pass too
+        self.launches_per_step = sum(self.launches_of(i) for i in range(len(self.shapes)))
+        self.flags = 0
         torch.cuda.synchronize()
 
     def call(self, i, r):
         M, N, K = self.shapes[i]
         c = (r * len(self.shapes) + i) % self.copies
-        self.a4w4.a4w4_gemm(self.A[self.slot][i], M, K, self.wq[(N, K)][c], self.ws[(N, K)][c], N,
-                            self.C[self.slot][i], self.work, self.ws_bytes)
+        self.a4w4.a4w4_gemm_ex(self.A[self.slot][i], M, K, self.wq[(N, K)][c], self.ws[(N, K)][c], N,
+                               self.C[self.slot][i], self.work, self.ws_bytes, self.flags)
 
     def step(self, r):
         for i in range(len(self.shapes)):
@@ -240,6 +263,10 @@ class DenseSweep:
     def kernel_name(self, i):
         M, N, K = self.shapes[i]
         return self.a4w4.a4w4_gemm_kernel_name(M, N, K)   # the library's own plan
+
+    def launches_of(self, i):
+        """Kernel launches of one call of GEMM i (the quantise-once plans add the pre-pass)."""
+        return 2 if "prequant" in self.kernel_name(i) else 1
 
     def label(self, i):
         M, N, K = self.shapes[i]
@@ -292,8 +319,10 @@ class MoeSweep:
                 q_host=[torch.empty((R, self.I // 2), dtype=torch.uint8).pin_memory() for _ in range(2)],
                 s_host=[torch.empty((R, self.I // 32), dtype=torch.uint8).pin_memory() for _ in range(2)]))
         self.slot = 0
+        self.flags = 0
         self.shapes = [(it["T"], 2 * self.I, self.D) for it in self.items]
-        self.launches_per_step = 4 * len(self.items)      # 3 sort kernels + GEMM1 per T
+        # 3 sort kernels + GEMM1 per T, + the token quantisation when GEMM1 has a workspace
+        self.launches_per_step = sum(4 + (1 if it["xws"] is not None else 0) for it in self.items)
         self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
         self.flops_per_step = sum(2 * it["T"] * self.topk * 2 * self.I * self.D for it in self.items)
         torch.cuda.synchronize()
@@ -340,6 +369,10 @@ class MoeSweep:
     def kernel_name(self, i):
         return "a4w4_gemm_kernel<moe,128>" if self.items[i]["xws"] is None else "a4w4_gemm_kernel<moe-prequant,128>"
 
+    def launches_of(self, i):
+        """Kernel launches of GEMM1 alone for token count i (+ the token quantisation)."""
+        return 1 if self.items[i]["xws"] is None else 2
+
     def label(self, i):
         return {"T": self.items[i]["T"], "E": self.E, "topk": self.topk, "D": self.D, "I": self.I}
 
@@ -355,41 +388,54 @@ def capture_graphs(torch, n, fn):
     return graphs
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-    import mxfp4_a4w4_gemm_gb300 as a4w4
-    from mxfp4_a4w4_gemm_gb300 import build
+def fp4_peak_tflops(peaks):
+    """Dense FP4 peak: the measured bf16 burst x the nominal fp4/bf16 ratio."""
+    return peaks["bf16_tflops"] * FP4_OVER_BF16
 
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local_rank if world > 1 else 0)
-    torch.cuda.set_device(dev)
-    build.build()
-    a4w4.lib()
-    if args.weight_prefetch:
-        a4w4.a4w4_set_weight_prefetch(1)
-    desc, shapes, family = WORKLOADS[args.workload]
-    if args.workload == "moe":
-        wl = MoeSweep(dev, inline=args.moe_inline)
-    else:
-        if args.shape:
-            shapes = [tuple(int(v) for v in args.shape.split(","))]
-            desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({args.workload} inputs)"
-        wl = DenseSweep(shapes, family, dev)
+
+def make_workload(name, args, dev):
+    desc, shapes, family = WORKLOADS[name]
+    if name == "moe":
+        return desc, MoeSweep(dev, inline=args.moe_inline)
+    if args.shape and args.workload != "all":
+        shapes = [tuple(int(v) for v in args.shape.split(","))]
+        desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({name} inputs)"
+    return desc, DenseSweep(shapes, family, dev)
+
+
+def time_step_graphs(torch, stream, graphs, steps, barrier, min_region_s=0.5):
+    """Median, over repeated timed regions of `steps` graph replays (at least
+    `min_region_s` of GPU time in all), of a region's milliseconds."""
+    n = len(graphs)
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    regions = []
+    t0 = time.time()
+    while True:
+        start.record(stream)
+        for i in range(steps):
+            graphs[i % n].replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        regions.append(start.elapsed_time(end))
+        if time.time() - t0 > min_region_s or len(regions) >= 50:
+            break
+    barrier()
+    return statistics.median(regions), len(regions)
+
+
+def measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, peak_src):
+    """Time one workload: graphs of whole steps (the value), per-GEMM launch
+    durations (roofline), end-to-end with host buffers (graph-pipelined and
+    eager).  Returns the workload's result block."""
     nrot = wl.copies
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
+    is_moe = isinstance(wl, MoeSweep)
     # warm the library's per-device set-up before any capture, then capture
     for r in range(2):
         wl.step(r)
     torch.cuda.synchronize()
     step_graphs = capture_graphs(torch, nrot, wl.step)
-
     # spin-up (>= 1 s untimed, brings clocks up) + W warm-up steps
     t0 = time.time()
     r = 0
@@ -401,35 +447,18 @@ def run_ours(args, rank, world, local_rank):
     for i in range(args.warmup):
         step_graphs[i % nrot].replay()
     torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
         time.sleep(0.25)
-        barrier()
-        torch.cuda.synchronize()
-        # keep the timed region >= 0.5 s for the clock samples: repeat whole timed
-        # regions of K steps and report the median region
-        regions = []
-        t_region = time.time()
-        while True:
-            start.record(stream)
-            for i in range(args.steps):
-                step_graphs[i % nrot].replay()
-            end.record(stream)
-            torch.cuda.synchronize()
-            regions.append(start.elapsed_time(end))
-            if time.time() - t_region > 0.5 or len(regions) >= 50:
-                break
-        barrier()
-    region_ms = max_over_ranks(statistics.median(regions), dev)
+        region_ms, nregions = time_step_graphs(torch, stream, step_graphs, args.steps, barrier)
+    region_ms = max_over_ranks(region_ms, dev)
     ms_per_step = region_ms / args.steps
     value = job_throughput(world, wl.bytes_per_step, ms_per_step)
+    launches = args.steps * wl.launches_per_step * nregions
+    del step_graphs
 
     # per-GEMM launch durations: one graph per shape of `nrot` back-to-back
     # launches on rotating weight copies, timed with events on this stream
     per = []
-    is_moe = isinstance(wl, MoeSweep)
     for i in range(len(wl.shapes)):
         # MoE: time GEMM1 alone (the sort's outputs for every routing are in place)
         g = capture_graphs(torch, 1, lambda _r, i=i: [
@@ -443,38 +472,62 @@ def run_ours(args, rank, world, local_rank):
             g.replay()
         s1.record(stream)
         torch.cuda.synchronize()
+        launches += reps * nrot * wl.launches_of(i)
+        del g
         us = s0.elapsed_time(s1) * 1e3 / (reps * nrot)
         M, N, K = wl.shapes[i]
         if is_moe:
             nbytes = sum(wl.item_bytes(i, rr) for rr in range(nrot)) / nrot
             nflops = 2 * M * wl.topk * N * K
+            pages = PAGES_MOE_US.get(M)
         else:
             nbytes, nflops = gemm_bytes(M, N, K), gemm_flops(M, N, K)
+            pages = PAGES_US.get((N, K, M))
         per.append(dict(wl.label(i), us=round(us, 3), tbs=round(nbytes / us / 1e6, 3),
-                        tflops=round(nflops / us / 1e6, 2), kernel=wl.kernel_name(i), bytes=int(nbytes)))
+                        tflops=round(nflops / us / 1e6, 2), kernel=wl.kernel_name(i), bytes=int(nbytes),
+                        flops=int(nflops), hbm_frac=round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4),
+                        fp4_frac=round(nflops / us / 1e6 / fp4_peak_tflops(peaks), 4),
+                        pages_mi355x_us=pages))
 
-    peaks, peak_src = load_peaks()
     # dominant kernel: the instantiation with the largest share of the step
     share = {}
     for p in per:
-        share.setdefault(p["kernel"], [0.0, 0, 0])
-        share[p["kernel"]][0] += p["us"]
-        share[p["kernel"]][1] += p["bytes"]
-        share[p["kernel"]][2] += 1
+        e = share.setdefault(p["kernel"], [0.0, 0, 0, 0])
+        e[0] += p["us"]
+        e[1] += p["bytes"]
+        e[2] += p["flops"]
+        e[3] += 1
     dom = max(share, key=lambda k: share[k][0])
-    dom_us, dom_bytes, dom_n = share[dom]
+    dom_us, dom_bytes, dom_flops, dom_n = share[dom]
     achieved_gbs = dom_bytes / (dom_us * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
+    roof_hbm = {"bound": "hbm", "kernel": dom, "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                "traffic": traffic_from_profiles(args.workload, dom), "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": traffic_from_profiles(name, dom), "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
                 "bytes_per_launch": round(dom_bytes / dom_n), "avg_launch_us": round(dom_us / dom_n, 3)}
+    block = {"workload": desc, "value": round(value, 4), "unit": "TB/s", "ms_per_step": round(ms_per_step, 5),
+             "tflops": round(world * wl.flops_per_step / (ms_per_step * 1e-3) / 1e12, 2),
+             "gemms_per_step": len(wl.shapes), "per_gemm": per, "roofline": roof_hbm,
+             "timed_regions": nregions, "clocks": clk.summary()}
+    if name == "large":
+        # the compute-bound end of the metric: FP4 tensor roofline over the
+        # GEMMs with M >= 512, the dominant kernel's launches
+        big = [p for p in per if p["M"] >= 512]
+        us = sum(p["us"] for p in big)
+        fl = sum(p["flops"] for p in big)
+        tf = fl / (us * 1e-6) / 1e12
+        pk = fp4_peak_tflops(peaks)
+        block["roofline"] = {
+            "bound": "tensor", "kernel": dom, "achieved": round(tf, 1), "peak": round(pk, 1), "unit": "TFLOP/s",
+            "frac": round(tf / pk, 4), "traffic": traffic_from_profiles(name, dom),
+            "peak_source": f"{peak_src} bf16_tflops x 13.5/2.25 (nominal dense fp4/bf16 ratio; of {peak_src})",
+            "gemms": "M >= 512", "avg_launch_us": round(us / len(big), 3)}
+        block["roofline_hbm"] = roof_hbm
 
-    # End to end through the C ABI with host buffers, pipelined as a serving
-    # loop would run it: step r's inputs go up on one copy stream and its
-    # outputs come back on another, in I/O slot r % 2, so step r+1's upload
-    # and step r-1's download overlap step r's kernels.  A slot is refilled
-    # only after the kernels of step r-2 stopped reading it and its outputs
-    # were read back; every step's copies lie inside the timed region.
+    # end to end, graphs: step r's inputs go up on one copy stream and its
+    # outputs come back on another, in I/O slot r % 2, so step r+1's upload and
+    # step r-1's download overlap step r's kernels.  A slot is refilled only
+    # after the kernels of step r-2 stopped reading it and its outputs were
+    # read back; every step's copies lie inside the timed region.
     e2e_graphs = []
     for r in range(2 * nrot):
         wl.slot = r % 2
@@ -484,13 +537,35 @@ def run_ours(args, rank, world, local_rank):
         e2e_graphs.append(g)
     wl.slot = 0
     torch.cuda.synchronize()
+    block["e2e"], n1 = e2e_pipelined(torch, stream, dev, wl, args.steps, barrier, world,
+                                     lambda r: e2e_graphs[r % len(e2e_graphs)].replay())
+    block["e2e"]["pipeline"] = "CUDA graphs of the C ABI calls; pinned host buffers, two I/O slots; H2D, kernels and D2H on three streams"
+    del e2e_graphs
+    # end to end, eager: every C ABI call issued from Python on every step
+    # (argument checks, planning, launch), same copies and pipelining
+    def eager(r):
+        wl.slot = r % 2
+        wl.step(r)
+    block["e2e_eager"], n2 = e2e_pipelined(torch, stream, dev, wl, args.steps, barrier, world, eager)
+    block["e2e_eager"]["pipeline"] = "every C ABI call issued from Python (ctypes) per step; pinned host buffers, two I/O slots, three streams"
+    wl.slot = 0
+    block["gpu_launches"] = launches + (n1 + n2) * wl.launches_per_step
+    status = wl.a4w4.a4w4_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {wl.a4w4.a4w4_strerror(status)}")
+    return block
+
+
+def e2e_pipelined(torch, stream, dev, wl, steps, barrier, world, run_step):
+    """Time `steps` end-to-end steps (H2D of the step's inputs, the step,
+    D2H of its outputs), pipelined over two I/O slots on three streams."""
     s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     up = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     down = [torch.cuda.Event() for _ in range(2)]
     used = [False, False]
 
-    def e2e_step(r):
+    def one(r):
         b = r % 2
         with torch.cuda.stream(s_up):
             if used[b]:
@@ -500,7 +575,7 @@ def run_ours(args, rank, world, local_rank):
         stream.wait_event(up[b])
         if used[b]:
             stream.wait_event(down[b])
-        e2e_graphs[r % len(e2e_graphs)].replay()
+        run_step(r)
         done[b].record(stream)
         with torch.cuda.stream(s_down):
             s_down.wait_event(done[b])
@@ -509,52 +584,100 @@ def run_ours(args, rank, world, local_rank):
         used[b] = True
 
     for r in range(4):
-        e2e_step(r)
+        one(r)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     s_up.wait_event(e0)
     s_down.wait_event(e0)
-    for r in range(args.steps):
-        e2e_step(r)
+    for r in range(steps):
+        one(r)
     for b in range(2):
         if used[b]:
             stream.wait_event(down[b])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    e2e_value = job_throughput(world, wl.bytes_per_step, e2e_ms)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, dev)
+    return ({"value": round(job_throughput(world, wl.bytes_per_step, ms), 4), "unit": "TB/s",
+             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": wl.h2d_bytes,
+             "d2h_bytes_per_step": wl.d2h_bytes}, steps + 4)
 
-    status = a4w4.a4w4_get_device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status}: {a4w4.a4w4_strerror(status)}")
 
-    pages_us = sum(PAGES_US.get((N, K, M), float("nan")) for M, N, K in wl.shapes)
-    vs = None
-    if args.workload == "decode" and world == 1:
-        vs = round(value / (wl.bytes_per_step / (pages_us * 1e-6) / 1e12), 3)
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mxfp4_a4w4_gemm_gb300 as a4w4
+    from mxfp4_a4w4_gemm_gb300 import build
 
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    a4w4.lib()
+    flags = a4w4.A4W4_GEMM_WEIGHT_PREFETCH if args.weight_prefetch else 0
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    names = ALL_WORKLOADS if args.workload == "all" else [args.workload]
+    blocks = {}
+    headline = names[0]
+    for name in names:
+        desc, wl = make_workload(name, args, dev)
+        wl.flags = flags
+        blocks[name] = measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, peak_src)
+        if name == "decode" and args.weight_prefetch:
+            # the same step without weight prefetch (each GEMM streams its
+            # weights only after the previous kernel completes)
+            wl.flags = 0
+            g = capture_graphs(torch, wl.copies, wl.step)
+            for i in range(args.warmup):
+                g[i % len(g)].replay()
+            ms, _ = time_step_graphs(torch, stream, g, args.steps, barrier, min_region_s=0.3)
+            ms = max_over_ranks(ms, dev) / args.steps
+            blocks[name]["no_weight_prefetch"] = {"value": round(job_throughput(world, wl.bytes_per_step, ms), 4),
+                                                  "unit": "TB/s", "ms_per_step": round(ms, 5)}
+            blocks[name]["gpu_launches"] += (args.warmup + args.steps) * wl.launches_per_step
+            del g
+        if name == "decode" and world == 1:
+            pages_us = sum(PAGES_US[(N, K, M)] for M, N, K in wl.shapes)
+            blocks[name]["vs_pages_mi355x"] = round(
+                blocks[name]["value"] / (wl.bytes_per_step / (pages_us * 1e-6) / 1e12), 3)
+        if rank == 0 and not args.no_cpu_baseline:
+            blocks[name]["cpu_baseline"] = cpu_baseline(name, budget_s=args.cpu_seconds)
+        del wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    h = blocks[headline]
     line = {
-        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": vs, "dtype": "e2m1 x e2m1 -> fp32 (bf16 in/out)",
+        "metric": METRIC, "value": h["value"], "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> fp32 (bf16 in/out)",
         "data": "synthetic (seeded; no checkpoints or datasets)",
-        "config": {"workload": desc, "gemms_per_step": len(wl.shapes), "graphs": "CUDA graphs, one per step",
+        "config": {"workload": h["workload"], "gemms_per_step": h["gemms_per_step"],
+                   "graphs": "CUDA graphs, one per step",
                    "weight_prefetch": bool(args.weight_prefetch),
-                   "l2": (f"{nrot} routings rotate (experts touched per step differ); W1 is 2.6 GB" if is_moe else
-                          f"weights rotate over {nrot} copies ({nrot * sum(gemm_bytes(0, N, K) for N, K in wl.wq) / 1e6:.0f} MB > 2x L2)"),
+                   "l2": "inputs larger than L2: weights rotate over copies > 2x L2 (MoE: 2.6 GB of experts)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "per_gemm": per, "timed_regions": len(regions)},
-        "roofline": roofline,
-        "e2e": {"value": round(e2e_value, 4), "unit": "TB/s", "ms_per_step": round(e2e_ms, 5),
-                "pipeline": "pinned host buffers, two I/O slots; H2D, kernels and D2H on three streams",
-                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes},
-        "gpu_launches": args.steps * wl.launches_per_step * len(regions),
-        "clocks": clk.summary(),
+                   "per_gemm": h["per_gemm"], "timed_regions": h["timed_regions"]},
+        "roofline": h["roofline"],
+        "e2e": h["e2e"],
+        "e2e_eager": h["e2e_eager"],
+        "gpu_launches": sum(b["gpu_launches"] for b in blocks.values()),
+        "clocks": h["clocks"],
     }
-    if rank == 0 and not args.no_cpu_baseline and not is_moe:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    for k in ("no_weight_prefetch", "vs_pages_mi355x", "cpu_baseline"):
+        if k in h:
+            line[k] = h[k]
+    if len(blocks) > 1:
+        line["configs"] = {k: {kk: vv for kk, vv in b.items()} for k, b in blocks.items() if k != headline}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -582,7 +705,8 @@ def traffic_from_profiles(workload, kernel):
 def oracle_sample_step(shapes, family, r, cols=16):
     """One bounded oracle step: for every GEMM of the workload, the oracle's
     full path (quantise A and a 16-row slice of W, float64 products, BF16
-    rounding) on the output columns n0..n0+15, n0 rotating with r."""
+    rounding) on the output columns n0..n0+15, n0 rotating with r.  Returns
+    the algorithmic bytes of that sample."""
     from oracle import gemm
     done = 0
     for i, (M, N, K) in enumerate(shapes):
@@ -590,6 +714,38 @@ def oracle_sample_step(shapes, family, r, cols=16):
         n0 = ((r * 7 + i) * cols) % N
         gemm.gemm_a4w4(A_bits, W_bits[n0:n0 + cols])
         done += cols * K // 2 + cols * K // 32 + 2 * M * K + 2 * M * cols
+    return done
+
+
+def oracle_quant_only(shapes, family, r, cols=16):
+    """The quantisation part of oracle_sample_step alone (A and the W slice)."""
+    from oracle import mxfp4
+    for i, (M, N, K) in enumerate(shapes):
+        A_bits, W_bits = _cached_problem(M, N, K, family)
+        n0 = ((r * 7 + i) * cols) % N
+        mxfp4.mxfp4_quant(A_bits)
+        mxfp4.mxfp4_quant(W_bits[n0:n0 + cols])
+
+
+_MOE_CACHE = {}
+
+
+def oracle_moe_sample(r, rows_per_t=1):
+    """One bounded oracle step of the MoE GEMM1 workload: for every token
+    count T, `rows_per_t` routed rows (rotating with r) through the oracle's
+    GEMM1 + SwiGLU + requant.  Returns the algorithmic bytes of the sample
+    (each row's expert weights, token and output)."""
+    from oracle import moe
+    c = workloads.MOE
+    E, topk, D, I = c["experts"], c["topk"], c["model_dim"], c["inter_dim"]
+    done = 0
+    for T in c["tokens"]:
+        if T not in _MOE_CACHE:
+            _MOE_CACHE[T] = (workloads.moe_tokens_bits(T, D), workloads.moe_topk_ids(T, E, topk))
+        X, ids = _MOE_CACHE[T]
+        rows = [(r * rows_per_t + j) * 7919 % (T * topk) for j in range(rows_per_t)]
+        moe.gemm1_rows(X, ids, lambda e: workloads.moe_expert_weight_bits(e, 2 * I, D), rows, I)
+        done += len(rows) * int(2 * I * D * (1 / 2 + 1 / 32) + 2 * D + I // 2 + I // 32)
     return done
 
 
@@ -615,43 +771,89 @@ def _threads():
         return os.cpu_count() or 1
 
 
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(workload, budget_s=15.0):
-    desc, shapes, family = WORKLOADS[workload]
-    for M, N, K in shapes:
-        _cached_problem(M, N, K, family)
-    oracle_sample_step(shapes, family, 0)
+    """The oracle as it stands, timed on this host's cores on a bounded sample
+    of `workload`: repeated sample steps for about `budget_s` seconds (the
+    value), plus quantisation and GEMM timed apart on one sample step (median
+    of 3 each)."""
+    if workload == "moe":
+        step, quant = oracle_moe_sample, None
+        sample = ("every token count's routed row per step through GEMM1 + SwiGLU + requant "
+                  "(each row's expert quantised in full)")
+    else:
+        desc, shapes, family = WORKLOADS[workload]
+        for M, N, K in shapes:
+            _cached_problem(M, N, K, family)
+        step = lambda r: oracle_sample_step(shapes, family, r)        # noqa: E731
+        quant = lambda r: oracle_quant_only(shapes, family, r)        # noqa: E731
+        sample = ("every GEMM of the workload on 16 output columns per step (full quantisation of A and of "
+                  "those W rows, float64 sums, BF16 rounding)")
+    step(0)
     t0 = time.time()
     done, r = 0, 0
     while time.time() - t0 < budget_s or r == 0:
-        done += oracle_sample_step(shapes, family, r)
+        done += step(r)
         r += 1
     dt = time.time() - t0
-    return {"value": round(done / dt / 1e12, 9), "unit": "TB/s", "cores": _threads(), "kind": "oracle",
-            "sample": f"{r} oracle steps over {dt:.1f} s; each step: every GEMM of the workload on 16 output "
-                      f"columns (full quantisation of A and of those W rows, float64 sums, BF16 rounding)"}
+    out = {"value": round(done / dt / 1e12, 9), "unit": "TB/s", "cores": _threads(), "kind": "oracle",
+           "cpu": cpu_model(), "nproc": os.cpu_count(),
+           "sample": f"{r} oracle steps over {dt:.1f} s; {sample}"}
+    if quant is not None:
+        full = []
+        qt = []
+        for _ in range(3):
+            t = time.perf_counter()
+            step(0)
+            full.append(time.perf_counter() - t)
+            t = time.perf_counter()
+            quant(0)
+            qt.append(time.perf_counter() - t)
+        out["quant_s"] = round(statistics.median(qt), 4)
+        out["gemm_s"] = round(max(0.0, statistics.median(full) - statistics.median(qt)), 4)
+        out["split"] = "one sample step, median of 3: quantisation of A and the W slice; the rest (products, sums, rounding)"
+    return out
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    desc, shapes, family = WORKLOADS[args.workload]
-    for M, N, K in shapes:
-        _cached_problem(M, N, K, family)
+    name = ALL_WORKLOADS[0] if args.workload == "all" else args.workload
+    desc, shapes, family = WORKLOADS[name]
+    if name == "moe":
+        step = oracle_moe_sample
+        sample = "every token count's routed row per step through the oracle's GEMM1 + SwiGLU + requant"
+    else:
+        for M, N, K in shapes:
+            _cached_problem(M, N, K, family)
+        step = lambda r: oracle_sample_step(shapes, family, r)        # noqa: E731
+        sample = "every GEMM of the workload on 16 output columns per step"
     for r in range(args.warmup):
-        oracle_sample_step(shapes, family, r)
+        step(r)
     t0 = time.time()
     done = 0
     for r in range(args.steps):
-        done += oracle_sample_step(shapes, family, r)
+        done += step(r)
     dt = time.time() - t0
     value = done / dt / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 9), "unit": "TB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": desc, "sample": "every GEMM of the workload on 16 output columns per step"},
+            "config": {"workload": desc, "sample": sample},
             "cpu_baseline": {"value": round(value, 9), "unit": "TB/s", "cores": _threads(), "kind": "oracle",
-                             "sample": f"{args.steps} oracle steps, 16 output columns of every GEMM per step"},
+                             "cpu": cpu_model(), "nproc": os.cpu_count(),
+                             "sample": f"{args.steps} oracle steps; {sample}"},
             "e2e": {"value": round(value, 9), "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -662,10 +864,11 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", choices=["all"] + sorted(WORKLOADS), default="all")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle baseline budget per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family")
+    ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family "
+                                                "(with a single --workload)")
     ap.add_argument("--moe-inline", action="store_true", help="MoE: quantise gathered rows inline in every tile")
     ap.add_argument("--no-weight-prefetch", dest="weight_prefetch", action="store_false",
                     help="do not let a GEMM stream its weights before the previous kernel finishes (default: "

@@ -103,6 +103,20 @@ int a4w4_gemm_kernel_name(int M, int N, int K, char* buf, size_t n);
 int a4w4_gemm(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
               void* C_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* a4w4_gemm with per-call options; a4w4_gemm(...) is a4w4_gemm_ex(..., 0, stream).
+ * Flags (unknown bits give A4W4_ERR_ARG):
+ *   A4W4_GEMM_WEIGHT_PREFETCH -- the GEMM is launched with programmatic
+ *     dependent launch like every GEMM here (it may start while the previous
+ *     kernel on `stream` still runs, and waits for that kernel before it
+ *     touches A, C or the workspace); with this flag it also starts streaming
+ *     Wq/Ws before that wait, hiding the weight fetch behind the previous
+ *     kernel.  Set it only when the kernel issued just before this call on
+ *     the same stream does not write Wq or Ws (weights prepared earlier and
+ *     left unchanged, as in inference).  The promise covers this call alone. */
+enum { A4W4_GEMM_WEIGHT_PREFETCH = 1 };
+int a4w4_gemm_ex(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
+                 void* C_bf16, void* workspace, size_t ws_bytes, unsigned int flags, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Standalone MXFP4 quantisation (plain layout).
  * "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Summary (the standalone quant
@@ -166,20 +180,25 @@ int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
 /* ------------------------------------------------------------------------ */
 /* Dense A4W4 GEMM that allocates nothing (no counterpart on the source pages:
  * it exists for callers of this library).  Same arguments and result as
- * a4w4_gemm() minus the workspace.  For callers that cannot allocate device
- * memory where they call the GEMM -- code under a framework allocator that owns
- * all device memory, or a latency-critical path that cannot afford cudaMalloc's
- * implicit synchronisation -- and so cannot hand a4w4_gemm() the split-K
- * workspace it needs at small M.
- *   Scratch: a fixed 16 MiB array inside the library's device image, present on
- *   every GPU that loads the library until the process exits.  A shape whose
- *   tile plan needs more (a4w4_gemm_workspace_bytes(M, N, K) > 16 MiB) is
- *   refused with A4W4_ERR_WORKSPACE.
- *   The first call on a device looks the array's device address up (once per
- *   device, with that device current); make that first call before any stream
- *   capture.  It calls no allocator.
+ * a4w4_gemm() minus the workspace: the same plan, kernels and reduction order,
+ * so the output is bit-identical.  For callers that cannot allocate device
+ * memory where they call the GEMM -- code under a framework allocator that
+ * owns all device memory, or a latency-critical path that cannot afford
+ * cudaMalloc's implicit synchronisation -- and so cannot hand a4w4_gemm() the
+ * workspace its plan needs for M > 64: the activations quantised once into
+ * MXFP4 tiles (64 < M <= 128 when N >= 4096, every M > 128) and, for M > 128,
+ * the fp32 split-K partial tiles and tile counters of a tile split over more
+ * CTAs than one cluster holds.  M <= 64 uses no scratch.
+ *   Scratch: a fixed 16 MiB array inside the library's device image.  It comes
+ *   into being on a device with the first a4w4_gemm_noalloc call there (the
+ *   CUDA runtime loads the library's device code lazily), which also looks up
+ *   its device address, whatever the shape; make that first call before any
+ *   stream capture.  It stays until the process exits.  No call allocates.
+ *   A plan needing more than 16 MiB (a4w4_gemm_workspace_bytes(M, N, K) >
+ *   16 MiB: at K = 7168, M above about 4,400 rows; or split-K partials such as
+ *   those of 200 x 1536 x 7168, 18 MiB) is refused with A4W4_ERR_WORKSPACE.
  *   All calls on a GPU share the array and it keeps the last call's contents:
- *   each call clears the tile counters it needs on `stream` first, and calls
+ *   each call clears the tile counters it uses on `stream` first, and calls
  *   that may run at the same time on one GPU (different streams) race on it --
  *   serialise them. */
 int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
@@ -192,17 +211,6 @@ int a4w4_get_device_status(void* stream);
 
 /* Static, human-readable name of a return code. */
 const char* a4w4_strerror(int code);
-
-/* Weight prefetch across kernel boundaries (default off).  GEMM kernels are
- * launched with programmatic dependent launch: a GEMM may start while the
- * previous kernel on its stream is still running, and it waits for that kernel
- * before touching activations, outputs or workspace.  With prefetch enabled it
- * also starts streaming its WEIGHTS (Wq, Ws, W1q, W1s) before that wait, which
- * hides the weight fetch latency behind the previous kernel.  Enable it only
- * when the kernel issued just before a GEMM on the same stream does not write
- * that GEMM's weights (weights prepared earlier and left unchanged, as in
- * inference).  Applies to launches issued after the call. */
-void a4w4_set_weight_prefetch(int enable);
 
 /* Override the in-kernel wait limit in nanoseconds (0 restores the default of
  * 2e8 ns).  Applies to launches issued after the call; used to test that an

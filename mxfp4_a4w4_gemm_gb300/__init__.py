@@ -8,10 +8,16 @@ device memory and streams.  Build the library with
 """
 
 from ._native import (  # noqa: F401
+    A4W4_GEMM_WEIGHT_PREFETCH,
     A4W4Error,
+    DEBUG_SIGNATURES,
     LIB_PATH,
     SIGNATURES,
+    a4w4_debug_gemm_activation_layout,
+    a4w4_debug_gemm_export,
+    a4w4_debug_moe_gemm1_export,
     a4w4_gemm,
+    a4w4_gemm_ex,
     a4w4_gemm_kernel_name,
     a4w4_gemm_noalloc,
     a4w4_gemm_workspace_bytes,
@@ -27,7 +33,6 @@ from ._native import (  # noqa: F401
     a4w4_mxfp4_quant,
     a4w4_prepare_gemm_weight,
     a4w4_set_wait_limit_ns,
-    a4w4_set_weight_prefetch,
     a4w4_strerror,
     a4w4_weight_codes_bytes,
     a4w4_weight_scales_bytes,

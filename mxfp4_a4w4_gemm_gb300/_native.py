@@ -25,6 +25,7 @@ SIGNATURES = {
     "a4w4_gemm_kernel_name": (_c_int, [_c_int, _c_int, _c_int, ctypes.c_char_p, _c_size]),
     "a4w4_workspace_init": (_c_int, [_vp, _c_size, _vp]),
     "a4w4_gemm": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, _vp]),
+    "a4w4_gemm_ex": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, ctypes.c_uint, _vp]),
     "a4w4_mxfp4_quant": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
     "a4w4_moe_w1_codes_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "a4w4_moe_w1_scales_bytes": (_c_size, [_c_int, _c_int, _c_int]),
@@ -38,9 +39,19 @@ SIGNATURES = {
     "a4w4_gemm_noalloc": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp]),
     "a4w4_get_device_status": (_c_int, [_vp]),
     "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
-    "a4w4_set_weight_prefetch": (None, [_c_int]),
     "a4w4_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
 }
+
+# test hooks of include/a4w4_debug.h (not the product API)
+_ip = ctypes.POINTER(ctypes.c_int)
+DEBUG_SIGNATURES = {
+    "a4w4_debug_gemm_activation_layout": (_c_int, [_c_int, _c_int, _c_int, _ip, _ip, _ip]),
+    "a4w4_debug_gemm_export": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, _vp, _c_size, _vp]),
+    "a4w4_debug_moe_gemm1_export": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int,
+                                             _c_int, _vp, _vp, _vp, _c_size, _vp, _c_size, _vp]),
+}
+
+A4W4_GEMM_WEIGHT_PREFETCH = 1
 
 _lib = None
 
@@ -59,7 +70,7 @@ def lib():
             raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
                                "(python -m mxfp4_a4w4_gemm_gb300.build)")
         L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
+        for name, (res, args) in list(SIGNATURES.items()) + list(DEBUG_SIGNATURES.items()):
             f = getattr(L, name)
             f.restype = res
             f.argtypes = args
@@ -129,6 +140,11 @@ def a4w4_gemm(A, M, K, Wq, Ws, N, C, workspace=None, ws_bytes=0, stream=None):
                                          ws_bytes, _stream(stream)))
 
 
+def a4w4_gemm_ex(A, M, K, Wq, Ws, N, C, workspace=None, ws_bytes=0, flags=0, stream=None):
+    _check("a4w4_gemm_ex", lib().a4w4_gemm_ex(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C), _ptr(workspace),
+                                               ws_bytes, flags, _stream(stream)))
+
+
 def a4w4_mxfp4_quant(X, rows, cols, q, scales, stream=None):
     _check("a4w4_mxfp4_quant", lib().a4w4_mxfp4_quant(_ptr(X), rows, cols, _ptr(q), _ptr(scales), _stream(stream)))
 
@@ -173,10 +189,12 @@ def a4w4_moe_gemm1(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1
 
 def a4w4_gemm_noalloc(A, M, K, Wq, Ws, N, C, stream=None):
     """a4w4_gemm without a workspace, for callers that cannot allocate device
-    memory at the call site: split-K scratch comes from a fixed 16 MiB array in
-    the library (shapes that need more raise A4W4Error, A4W4_ERR_WORKSPACE).
-    Make the first call on a device before any CUDA graph capture; calls that
-    may overlap on one GPU share the array and must be serialised."""
+    memory at the call site: the plan's scratch (activation tiles quantised
+    once, split-K partials and counters; only for M > 64) comes from a fixed
+    16 MiB array in the library (shapes that need more raise A4W4Error,
+    A4W4_ERR_WORKSPACE).  Make the first call on a device before any CUDA
+    graph capture; calls that may overlap on one GPU share the array and must
+    be serialised."""
     _check("a4w4_gemm_noalloc", lib().a4w4_gemm_noalloc(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C),
                                                          _stream(stream)))
 
@@ -186,11 +204,30 @@ def a4w4_get_device_status(stream=None):
     return lib().a4w4_get_device_status(_stream(stream))
 
 
-def a4w4_set_weight_prefetch(enable):
-    """Let GEMMs start streaming weights before the previous kernel on the
-    stream finishes (only if that kernel does not write those weights)."""
-    lib().a4w4_set_weight_prefetch(1 if enable else 0)
-
-
 def a4w4_set_wait_limit_ns(ns):
     lib().a4w4_set_wait_limit_ns(int(ns))
+
+
+# ---------------------------------------------------------------------------
+# test hooks (include/a4w4_debug.h)
+
+def a4w4_debug_gemm_activation_layout(M, N, K):
+    """(tile_rows, x_tiles, k_tiles) of a4w4_gemm(M, N, K)'s activation tiles."""
+    r, x, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check("a4w4_debug_gemm_activation_layout",
+           lib().a4w4_debug_gemm_activation_layout(M, N, K, ctypes.byref(r), ctypes.byref(x), ctypes.byref(k)))
+    return r.value, x.value, k.value
+
+
+def a4w4_debug_gemm_export(A, M, K, Wq, Ws, N, C, workspace, ws_bytes, dump, dump_bytes, stream=None):
+    _check("a4w4_debug_gemm_export",
+           lib().a4w4_debug_gemm_export(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C), _ptr(workspace), ws_bytes,
+                                        _ptr(dump), dump_bytes, _stream(stream)))
+
+
+def a4w4_debug_moe_gemm1_export(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
+                                ws, ws_bytes, dump, dump_bytes, stream=None):
+    _check("a4w4_debug_moe_gemm1_export",
+           lib().a4w4_debug_moe_gemm1_export(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert), _ptr(num_blocks),
+                                             topk, _ptr(W1q), _ptr(W1s), E, I, _ptr(out_q), _ptr(out_s), _ptr(ws),
+                                             ws_bytes, _ptr(dump), dump_bytes, _stream(stream)))

@@ -5,6 +5,7 @@
 #include <cstdio>
 
 #include "a4w4.h"
+#include "a4w4_debug.h"
 #include "launch.h"
 
 // Device status word: bit 0 set by a kernel whose bounded wait expired.
@@ -16,7 +17,6 @@ namespace {
 
 constexpr unsigned long long kDefaultWaitNs = 200000000ull;   // 0.2 s
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
-std::atomic<int> g_weight_prefetch{0};
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_sms[kMaxDevices];      // 0 = unknown, -1 = unsupported, else SM count
@@ -76,8 +76,52 @@ namespace a4w4 {
 int device_sms() { return current_device_sms(); }
 unsigned int* device_status_ptr() { return status_ptr(); }
 unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
-int weight_prefetch() { return g_weight_prefetch.load(std::memory_order_relaxed); }
 }  // namespace a4w4
+
+namespace {
+
+// Shared body of a4w4_gemm_ex and the activation-export test hook.
+int gemm_impl(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N, void* C_bf16,
+              void* workspace, size_t ws_bytes, unsigned int flags, void* stream, a4w4::ActDump dump) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0) return A4W4_ERR_ARG;
+  if (!aligned16(A_bf16) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(C_bf16)) return A4W4_ERR_ARG;
+  if ((flags & ~static_cast<unsigned int>(A4W4_GEMM_WEIGHT_PREFETCH)) != 0) return A4W4_ERR_ARG;
+  const int sms = current_device_sms();
+  if (sms < 0) return sms;
+  const a4w4::GemmPlan plan = a4w4::plan_gemm(M, N, K, sms);
+  if (plan.ws_bytes > 0 && (ws_bytes < plan.ws_bytes || !aligned16(workspace))) return A4W4_ERR_WORKSPACE;
+  unsigned int* status = status_ptr();
+  if (status == nullptr) return A4W4_ERR_LAUNCH;
+  return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, as_stream(stream),
+                           g_wait_ns.load(std::memory_order_relaxed), status,
+                           (flags & A4W4_GEMM_WEIGHT_PREFETCH) ? 1 : 0, dump);
+}
+
+int moe_gemm1_impl(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
+                   const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
+                   void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream, a4w4::ActDump dump) {
+  if (T <= 0 || D <= 0 || topk <= 0 || E <= 0 || I <= 0 || I % 128 != 0 || D % 128 != 0) return A4W4_ERR_ARG;
+  if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
+  if (!aligned16(X_bf16) || !aligned16(W1q) || !aligned16(W1s) || !aligned16(out_q) || out_s == nullptr ||
+      sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr)
+    return A4W4_ERR_ARG;
+  const int sms = current_device_sms();
+  if (sms < 0) return sms;
+  const int max_blocks = a4w4_moe_max_blocks(T, topk, E, 128);
+  if (max_blocks > 65535) return A4W4_ERR_ARG;
+  unsigned int* status = status_ptr();
+  if (status == nullptr) return A4W4_ERR_LAUNCH;
+  void* xq = nullptr;
+  if (ws != nullptr || ws_bytes != 0) {
+    if (!aligned16(ws) || ws_bytes < a4w4_moe_gemm1_workspace_bytes(T, D)) return A4W4_ERR_WORKSPACE;
+    xq = ws;
+  }
+  return a4w4::launch_moe_gemm1(X_bf16, T, D, sorted_rows, block_expert, num_blocks, max_blocks, topk, W1q, W1s,
+                                E, I, out_q, out_s, xq, as_stream(stream), g_wait_ns.load(std::memory_order_relaxed),
+                                status, sms, dump);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -122,18 +166,14 @@ int a4w4_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
   return cudaMemsetAsync(workspace, 0, ws_bytes, as_stream(stream)) == cudaSuccess ? A4W4_OK : A4W4_ERR_LAUNCH;
 }
 
+int a4w4_gemm_ex(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N, void* C_bf16,
+                 void* workspace, size_t ws_bytes, unsigned int flags, void* stream) {
+  return gemm_impl(A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, ws_bytes, flags, stream, a4w4::ActDump{});
+}
+
 int a4w4_gemm(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N, void* C_bf16,
               void* workspace, size_t ws_bytes, void* stream) {
-  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0) return A4W4_ERR_ARG;
-  if (!aligned16(A_bf16) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(C_bf16)) return A4W4_ERR_ARG;
-  const int sms = current_device_sms();
-  if (sms < 0) return sms;
-  const a4w4::GemmPlan plan = a4w4::plan_gemm(M, N, K, sms);
-  if (plan.ws_bytes > 0 && (ws_bytes < plan.ws_bytes || !aligned16(workspace))) return A4W4_ERR_WORKSPACE;
-  unsigned int* status = status_ptr();
-  if (status == nullptr) return A4W4_ERR_LAUNCH;
-  return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, as_stream(stream),
-                           g_wait_ns.load(std::memory_order_relaxed), status);
+  return gemm_impl(A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, ws_bytes, 0u, stream, a4w4::ActDump{});
 }
 
 int a4w4_mxfp4_quant(const void* X_bf16, int rows, int cols, void* q, void* scales, void* stream) {
@@ -196,25 +236,58 @@ size_t a4w4_moe_gemm1_workspace_bytes(int T, int D) {
 int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                    const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
                    void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream) {
-  if (T <= 0 || D <= 0 || topk <= 0 || E <= 0 || I <= 0 || I % 128 != 0 || D % 128 != 0) return A4W4_ERR_ARG;
-  if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
-  if (!aligned16(X_bf16) || !aligned16(W1q) || !aligned16(W1s) || !aligned16(out_q) || out_s == nullptr ||
-      sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr)
-    return A4W4_ERR_ARG;
+  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
+                        ws, ws_bytes, stream, a4w4::ActDump{});
+}
+
+// ---------------------------------------------------------------------------
+// Test hooks (a4w4_debug.h)
+
+int a4w4_debug_gemm_activation_layout(int M, int N, int K, int* tile_rows, int* x_tiles, int* k_tiles) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0) return A4W4_ERR_ARG;
+  if (tile_rows == nullptr || x_tiles == nullptr || k_tiles == nullptr) return A4W4_ERR_ARG;
+  const a4w4::GemmPlan pl = a4w4::plan_gemm(M, N, K, sizing_sms());
+  *tile_rows = pl.nx;
+  *x_tiles = pl.x_tiles;
+  *k_tiles = pl.kt;
+  return A4W4_OK;
+}
+
+int a4w4_debug_gemm_export(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N, void* C_bf16,
+                           void* workspace, size_t ws_bytes, void* dump, size_t dump_bytes, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0 || !aligned16(dump)) return A4W4_ERR_ARG;
   const int sms = current_device_sms();
   if (sms < 0) return sms;
-  const int max_blocks = a4w4_moe_max_blocks(T, topk, E, 128);
-  if (max_blocks > 65535) return A4W4_ERR_ARG;
-  unsigned int* status = status_ptr();
-  if (status == nullptr) return A4W4_ERR_LAUNCH;
-  void* xq = nullptr;
-  if (ws != nullptr || ws_bytes != 0) {
-    if (!aligned16(ws) || ws_bytes < a4w4_moe_gemm1_workspace_bytes(T, D)) return A4W4_ERR_WORKSPACE;
-    xq = ws;
-  }
-  return a4w4::launch_moe_gemm1(X_bf16, T, D, sorted_rows, block_expert, num_blocks, max_blocks, topk, W1q, W1s,
-                                E, I, out_q, out_s, xq, as_stream(stream), g_wait_ns.load(std::memory_order_relaxed),
-                                status, sms);
+  const a4w4::GemmPlan pl = a4w4::plan_gemm(M, N, K, sms);
+  const size_t atoms = static_cast<size_t>(pl.x_tiles) * pl.kt;
+  const size_t code_bytes = atoms * pl.nx * 128;
+  if (dump_bytes < code_bytes + atoms * 1024) return A4W4_ERR_ARG;
+  const cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(dump, 0, code_bytes + atoms * 1024, st) != cudaSuccess) return A4W4_ERR_LAUNCH;
+  a4w4::ActDump d{static_cast<uint8_t*>(dump), static_cast<uint8_t*>(dump) + code_bytes};
+  // the quantise-once plans build their tiles in the workspace, not in the
+  // producers: copy those out after the GEMM instead
+  const int rc = gemm_impl(A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, ws_bytes, 0u, stream,
+                           pl.prequant ? a4w4::ActDump{} : d);
+  if (rc != A4W4_OK || !pl.prequant) return rc;
+  const uint8_t* w8 = static_cast<const uint8_t*>(workspace);
+  if (cudaMemcpyAsync(d.codes, w8, atoms * 16384, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d.scales, w8 + atoms * 16384, atoms * 1024, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return A4W4_ERR_LAUNCH;
+  return A4W4_OK;
+}
+
+int a4w4_debug_moe_gemm1_export(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
+                                const int32_t* block_expert, const int32_t* num_blocks, int topk, const void* W1q,
+                                const void* W1s, int E, int I, void* out_q, void* out_s, void* ws, size_t ws_bytes,
+                                void* dump, size_t dump_bytes, void* stream) {
+  if (T <= 0 || D <= 0 || topk <= 0 || E <= 0 || D % 128 != 0 || !aligned16(dump)) return A4W4_ERR_ARG;
+  const size_t atoms = static_cast<size_t>(a4w4_moe_max_blocks(T, topk, E, 128)) * ((D + 255) / 256);
+  if (dump_bytes < atoms * (16384 + 1024)) return A4W4_ERR_ARG;
+  if (cudaMemsetAsync(dump, 0, atoms * (16384 + 1024), as_stream(stream)) != cudaSuccess) return A4W4_ERR_LAUNCH;
+  a4w4::ActDump d{static_cast<uint8_t*>(dump), static_cast<uint8_t*>(dump) + atoms * 16384};
+  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
+                        ws, ws_bytes, stream, d);
 }
 
 int a4w4_get_device_status(void* stream) {
@@ -237,8 +310,6 @@ const char* a4w4_strerror(int code) {
     default: return "unknown error";
   }
 }
-
-void a4w4_set_weight_prefetch(int enable) { g_weight_prefetch.store(enable ? 1 : 0, std::memory_order_relaxed); }
 
 void a4w4_set_wait_limit_ns(unsigned long long ns) {
   g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);

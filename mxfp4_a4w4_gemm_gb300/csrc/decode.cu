@@ -51,6 +51,10 @@ struct DecodeArgs {
   int prefetch_w;      // 1: weights may be read before the previous grid on the stream completes
   unsigned long long wait_ns;
   unsigned int* status;
+  // test hook (ActDump): the CTAs of weight tile 0 also store the activation
+  // tiles their producers build; nullptr in every product call
+  uint8_t* dump_codes;
+  uint8_t* dump_scales;
 };
 
 template <int NX, int SW, int SX>
@@ -264,6 +268,7 @@ __global__ void __launch_bounds__(DCfg<NX, SW, SX>::THREADS, DCfg<NX, SW, SX>::M
     constexpr int P = Cf::QWARPS * 32;
     constexpr int CH = Cf::A_CHUNK;
     const int blk = mvalid * 8;                    // valid blocks per stage
+    const bool dump = p.dump_codes != nullptr && w_tile == 0;
     bool stop = false;
     for (int r0 = 0, rnd = 0; r0 < nk && !stop; r0 += SX, ++rnd) {
       const int ns = nk - r0 < SX ? nk - r0 : SX;
@@ -308,9 +313,17 @@ __global__ void __launch_bounds__(DCfg<NX, SW, SX>::THREADS, DCfg<NX, SW, SX>::M
             uint8_t* xs = smem + Cf::OFF_XSF + j * Cf::XSF_STAGE;
             uint32_t code[4];
             const uint32_t e = quant32_bf16(w[c], code);
-            *reinterpret_cast<uint4*>(xt + (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4)) =
-                make_uint4(code[0], code[1], code[2], code[3]);
-            xs[(kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(e);
+            const uint32_t code_off = (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4);
+            const uint32_t sf_off = (kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+            const uint4 cv = make_uint4(code[0], code[1], code[2], code[3]);
+            *reinterpret_cast<uint4*>(xt + code_off) = cv;
+            xs[sf_off] = static_cast<uint8_t>(e);
+            if (dump) {
+              // test hook: the same bytes at the same offsets of a global copy
+              const long long atom = static_cast<long long>(x_tile) * p.KT + kt0 + r0 + j;
+              *reinterpret_cast<uint4*>(p.dump_codes + atom * Cf::X_STAGE + code_off) = cv;
+              p.dump_scales[atom * Cf::XSF_STAGE + sf_off] = static_cast<uint8_t>(e);
+            }
           }
         }
       }
@@ -465,7 +478,7 @@ static int launch_decode_cfg(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
 }
 
 int launch_decode(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
-                  cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
+                  cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w, ActDump dump) {
   if (pl.splits < 1 || pl.splits > 16) return -4;   // push buffer and cluster limits
   DecodeArgs a{};
   a.A = static_cast<const uint16_t*>(A);
@@ -473,7 +486,9 @@ int launch_decode(const GemmPlan& pl, const void* A, int M, int K, const void* W
   a.Ws = static_cast<const uint8_t*>(Ws);
   a.C = static_cast<uint16_t*>(C);
   a.M = M; a.N = N; a.K = K; a.KT = pl.kt; a.splits = pl.splits;
-  a.prefetch_w = weight_prefetch();
+  a.prefetch_w = prefetch_w;
+  a.dump_codes = dump.codes;
+  a.dump_scales = dump.scales;
   a.wait_ns = wait_ns;
   a.status = status;
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);

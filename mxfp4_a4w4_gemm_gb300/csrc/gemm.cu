@@ -57,6 +57,10 @@ struct GemmArgs {
   long long expert_code_bytes, expert_sf_bytes;
   uint8_t* out_q;
   uint8_t* out_s;
+  // test hook (ActDump): the CTAs of weight tile 0 also store the activation
+  // tiles their producers build; nullptr in every product call
+  uint8_t* dump_codes;
+  uint8_t* dump_scales;
 };
 
 constexpr int kRedStride = 260;      // floats per staged row of a 128x256 partial (1040 bytes)
@@ -356,8 +360,17 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         }
       }
     };
-    // Quantise them into the stage's swizzled operand tile and scale atom.
-    auto quant_stage = [&](int s, const uint32_t (&w)[PER][16]) {
+    // Test hook: the CTAs of weight tile 0 store each code chunk and scale
+    // byte at the same offsets in a global copy of the tile as well.
+    const bool dump = p.dump_codes != nullptr && w_tile == 0;
+    auto dump_store = [&](int i, uint32_t code_off, uint32_t sf_off, uint4 c, uint32_t e) {
+      const long long atom = static_cast<long long>(x_tile) * p.KT + kt0 + i;
+      *reinterpret_cast<uint4*>(p.dump_codes + atom * Cf::X_CODE_BYTES + code_off) = c;
+      p.dump_scales[atom * Cf::X_SF_BYTES + sf_off] = static_cast<uint8_t>(e);
+    };
+    // Quantise them into stage i's swizzled operand tile and scale atom.
+    auto quant_stage = [&](int i, const uint32_t (&w)[PER][16]) {
+      const int s = i % STAGES;
       uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
       uint8_t* xs = smem + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
 #pragma unroll
@@ -367,9 +380,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           const int r = j >> 3, kb = j & 7;
           uint32_t c[4];
           const uint32_t e = quant32_bf16(w[u], c);
-          *reinterpret_cast<uint4*>(xt + (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4)) =
-              make_uint4(c[0], c[1], c[2], c[3]);
-          xs[(kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(e);
+          const uint32_t code_off = (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4);
+          const uint32_t sf_off = (kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+          const uint4 cv = make_uint4(c[0], c[1], c[2], c[3]);
+          *reinterpret_cast<uint4*>(xt + code_off) = cv;
+          xs[sf_off] = static_cast<uint8_t>(e);
+          if (dump) dump_store(i, code_off, sf_off, cv, e);
         }
       }
       fence_proxy_async_smem();
@@ -393,7 +409,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           }
         }
       };
-      auto gstore = [&](int s, const uint4 (&c)[PER], const uint32_t (&e)[PER]) {
+      auto gstore = [&](int i, const uint4 (&c)[PER], const uint32_t (&e)[PER]) {
+        const int s = i % STAGES;
         uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
         uint8_t* xs = smem + Cf::OFF_XSF + s * Cf::X_SF_BYTES;
 #pragma unroll
@@ -401,8 +418,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           const int j = qt + u * P;
           if (j < Cf::BLOCKS_PER_STAGE && rvalid[u]) {
             const int r = j >> 3, kb = j & 7;
-            *reinterpret_cast<uint4*>(xt + (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4)) = c[u];
-            xs[(kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3)] = static_cast<uint8_t>(e[u]);
+            const uint32_t code_off = (r >> 3) * 1024 + (r & 7) * 128 + ((kb ^ (r & 7)) << 4);
+            const uint32_t sf_off = (kb >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb & 3);
+            *reinterpret_cast<uint4*>(xt + code_off) = c[u];
+            xs[sf_off] = static_cast<uint8_t>(e[u]);
+            if (dump) dump_store(i, code_off, sf_off, c[u], e[u]);
           }
         }
         fence_proxy_async_smem();
@@ -414,12 +434,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       for (int i = 0; i < nq; i += 2) {
         if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
         if (i + 1 < nq) gload(i + 1, cb, eb);
-        gstore(i % STAGES, ca, ea);
+        gstore(i, ca, ea);
         if (i + 1 >= nq) break;
         const int i1 = i + 1;
         if (!mbar_wait(empty(i1 % STAGES), ((i1 / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
         if (i1 + 1 < nq) gload(i1 + 1, ca, ea);
-        gstore(i1 % STAGES, cb, eb);
+        gstore(i1, cb, eb);
       }
     } else if (PER <= 2) {
       // A register ring: the loads of stages i+1 .. i+R-1 are in flight while
@@ -440,7 +460,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
             stop = true;
             break;
           }
-          quant_stage(i % STAGES, wr[r]);
+          quant_stage(i, wr[r]);
           if (i + R < nq) load_stage(i + R, wr[r]);
         }
       }
@@ -449,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
         uint32_t w[PER][16];
         load_stage(i, w);
-        quant_stage(i % STAGES, w);
+        quant_stage(i, w);
       }
     }
 
@@ -848,9 +868,12 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
 }
 
 int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
-                void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
+                void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w,
+                ActDump dump) {
   GemmArgs a{};
-  a.prefetch_w = weight_prefetch();
+  a.prefetch_w = prefetch_w;
+  a.dump_codes = dump.codes;
+  a.dump_scales = dump.scales;
   a.status = status;
   a.A = static_cast<const uint16_t*>(A);
   a.Wq = static_cast<const uint8_t*>(Wq);
@@ -870,7 +893,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   a.cluster_reduce = pl.cluster_reduce;
   a.wait_ns = wait_ns;
   const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
-  if (pl.decode) return launch_decode(pl, A, M, K, Wq, Ws, N, C, st, wait_ns, status);
+  if (pl.decode) return launch_decode(pl, A, M, K, Wq, Ws, N, C, st, wait_ns, status, prefetch_w, dump);
   if (pl.swap_ab) {
     switch (pl.nx) {
       case 32: return launch_cfg<kSwap, 32, 4>(a, grid, st);
@@ -891,9 +914,11 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s, int E,
                      int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st, unsigned long long wait_ns,
-                     unsigned int* status, int sms) {
+                     unsigned int* status, int sms, ActDump dump) {
   GemmArgs a{};
   a.status = status;
+  a.dump_codes = dump.codes;
+  a.dump_scales = dump.scales;
   a.A = static_cast<const uint16_t*>(X);
   a.Wq = static_cast<const uint8_t*>(W1q);
   a.Ws = static_cast<const uint8_t*>(W1s);

@@ -50,22 +50,35 @@ int ensure_func_attrs(std::atomic<unsigned long long>& done, SetFn set) {
 int device_sms();
 unsigned int* device_status_ptr();
 unsigned long long wait_limit_ns();
-int weight_prefetch();
+
+// Test hook (a4w4_debug.h): where the activation producers of the CTAs of
+// weight tile 0 also store the MXFP4 operand tiles they build in shared
+// memory.  Atom a = x_tile * KT + kt: codes at codes + a * (rows per tile *
+// 128) in the swizzled tile layout, scales at scales + a * 1024 in the
+// scale-atom layout.  codes == nullptr: off (every product call).
+struct ActDump {
+  uint8_t* codes;
+  uint8_t* scales;
+};
 
 int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms);
 int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
                           cudaStream_t st, int sms);
 // A [M, K] -> MXFP4 in the weight tile layout (rows padded to 128 with zeros).
 int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms);
+// prefetch_w: weights may be read before the previous grid on the stream
+// completes (the caller guarantees that grid does not write them).
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
-                void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
+                void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status,
+                int prefetch_w, ActDump dump);
 // plan.decode: the decode kernel (decode.cu); no workspace.
 int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
-                  void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
+                  void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w,
+                  ActDump dump);
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s,
                      int E, int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
-                     unsigned long long wait_ns, unsigned int* status, int sms);
+                     unsigned long long wait_ns, unsigned int* status, int sms, ActDump dump);
 int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
                     int32_t* block_expert, int32_t* num_blocks, void* ws, cudaStream_t st);
 size_t moe_sort_ws_bytes(int T, int topk, int E);

@@ -1,19 +1,28 @@
 // noalloc.cu -- a dense A4W4 GEMM entry point that allocates nothing.
 //
-// a4w4_gemm() needs a caller-allocated workspace whenever it splits K across
-// the SMs (small M).  Some callers cannot provide one: code that runs under a
-// framework allocator owning all device memory, or a latency-critical path
-// where cudaMalloc's implicit synchronisation is not acceptable.  This entry
-// point runs the same GEMM with its split-K scratch (fp32 partial tiles and
-// tile counters) in a fixed array that is part of the library's device image.
+// a4w4_gemm() takes a caller-allocated workspace whenever its tile plan needs
+// one: for M > 64 (64 < M <= 128 when N >= 4096; every M > 128) the activations
+// are quantised once into MXFP4 tiles there, and for M > 128 a tile whose K
+// range is split over more CTAs than one thread-block cluster holds also keeps
+// its fp32 partial tiles and a tile counter there.  M <= 64 needs none.  Some
+// callers cannot provide that memory: code running under a framework allocator
+// that owns all device memory, or a latency-critical path where cudaMalloc's
+// implicit device synchronisation is not acceptable.  This entry point runs the
+// same plan and kernels with that scratch in a fixed array that belongs to the
+// library's device image.
 //
-// The array is kNoAllocScratchBytes (16 MiB) on every GPU that loads the
-// library, kept until the process exits.  A call whose tile plan needs more
-// scratch than that is refused with A4W4_ERR_WORKSPACE.  All calls on a GPU
-// share its array, which keeps whatever the last call left there: the tile
-// counters are cleared at the start of every call, and calls that can run at
-// the same time on one GPU (issued on different streams) race on the array,
-// so the caller must serialise them.
+// The array holds kNoAllocScratchBytes (16 MiB).  It comes into being on a
+// device when this file's module is loaded there, which with the CUDA
+// runtime's lazy module loading is the first call of a4w4_gemm_noalloc on
+// that device (the call that looks its address up), and stays until the
+// process exits.  A plan that needs more than 16 MiB is refused with
+// A4W4_ERR_WORKSPACE; at K = 7168 that is M beyond about 4,400 rows (487 KB of
+// activation tiles per 128 rows), and shapes such as 200 x 1536 x 7168 whose
+// K split needs 18 MiB of partial tiles.  Every call shares the array, which
+// keeps whatever the previous call left there: the tile counters are cleared
+// on `stream` at the start of each call that uses them (the activation tiles
+// and partials are overwritten before they are read), and calls that can run
+// at the same time on one GPU (issued on different streams) race on it.
 #include <atomic>
 #include <cstdint>
 
@@ -28,9 +37,9 @@ static __device__ __align__(256) unsigned char g_gemm_scratch[kNoAllocScratchByt
 constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-// Device address of g_gemm_scratch on the current device.  Host code only
-// sees a host-side stand-in under that name, so the real address is looked up
-// once per device (with that device current) and cached.
+// Device address of g_gemm_scratch on the current device.  In host code the
+// array's name denotes a host-side stand-in, not device memory, so the real
+// address is looked up once per device (with that device current) and cached.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -54,24 +63,25 @@ int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const vo
   if (!aligned16(A_bf16) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(C_bf16)) return A4W4_ERR_ARG;
   const int sms = a4w4::device_sms();
   if (sms < 0) return sms;
+  // Looked up on every call, whatever the shape, so that the first call on a
+  // device -- the one to make before any stream capture -- does the set-up
+  // even when its own plan needs no scratch.
+  void* scratch = scratch_address();
+  if (scratch == nullptr) return A4W4_ERR_LAUNCH;
   const a4w4::GemmPlan plan = a4w4::plan_gemm(M, N, K, sms);
   if (plan.ws_bytes > kNoAllocScratchBytes) return A4W4_ERR_WORKSPACE;
   unsigned int* status = a4w4::device_status_ptr();
   if (status == nullptr) return A4W4_ERR_LAUNCH;
-  void* scratch = nullptr;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (plan.ws_bytes > 0) {
-    scratch = scratch_address();
-    if (scratch == nullptr) return A4W4_ERR_LAUNCH;
-    // The split-K tile counters must start at zero; a previous call (or one
-    // that timed out) may have left them otherwise.  They follow the
-    // activation tiles and the partials in the scratch layout.
-    const size_t counters = plan.aq_bytes + plan.partial_bytes;
-    if (plan.ws_bytes > counters &&
-        cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters, 0, plan.ws_bytes - counters, st) != cudaSuccess)
-      return A4W4_ERR_LAUNCH;
-  }
-  return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, scratch, st, a4w4::wait_limit_ns(), status);
+  // The split-K tile counters must start at zero; an earlier call (or one
+  // that timed out) may have left them otherwise.  They follow the activation
+  // tiles and the partial tiles in the scratch layout.
+  const size_t counters = plan.aq_bytes + plan.partial_bytes;
+  if (plan.ws_bytes > counters &&
+      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters, 0, plan.ws_bytes - counters, st) != cudaSuccess)
+    return A4W4_ERR_LAUNCH;
+  return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, plan.ws_bytes > 0 ? scratch : nullptr, st,
+                           a4w4::wait_limit_ns(), status, 0, a4w4::ActDump{});
 }
 
 }  // extern "C"

@@ -17,29 +17,38 @@ def host_bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def unshuffle_weight(wq, ws, N, K):
-    """Read the preshuffled weight layout of include/a4w4.h back into plain
-    row-major packed codes [N, K/2] and E8M0 scales [N, K/32].
+def unshuffle_tiles(codes, scales, rows, tiles, KT):
+    """Read tiles of `rows` rows x 256 K in the swizzled operand layout of
+    include/a4w4.h (codes: atom a = tile * KT + kt of rows * 128 bytes, byte b
+    of row r at (r/8)*1024 + (r%8)*128 + ((b/16) ^ (r%8))*16 + b%16; scales:
+    1024 bytes per atom, 32-block j of row r at (j/4)*512 + (r%32)*16 +
+    (r/32)*4 + j%4) back into plain row-major packed codes [tiles*rows, KT*128]
+    and E8M0 scales [tiles*rows, KT*8].
 
     Written from the header's formulas, independently of the CUDA code.
     """
-    KP = -(-K // 256) * 256
-    KT = KP // 256
-    wq = np.asarray(wq, dtype=np.uint8).reshape(N // 128, KT, 16384)
-    ws = np.asarray(ws, dtype=np.uint8).reshape(N // 128, KT, 1024)
-    n = np.arange(N)
-    nt, r = n // 128, n % 128
+    codes = np.asarray(codes, dtype=np.uint8)[:tiles * KT * rows * 128].reshape(tiles, KT, rows * 128)
+    scales = np.asarray(scales, dtype=np.uint8)[:tiles * KT * 1024].reshape(tiles, KT, 1024)
+    n = np.arange(tiles * rows)
+    nt, r = n // rows, n % rows
     b = np.arange(128)
-    codes = np.empty((N, KP // 2), dtype=np.uint8)
+    out_c = np.empty((tiles * rows, KT * 128), dtype=np.uint8)
+    off = (r[:, None] // 8) * 1024 + (r[:, None] % 8) * 128 + (((b[None, :] // 16) ^ (r[:, None] % 8)) * 16) + b[None, :] % 16
     for kt in range(KT):
-        off = (r[:, None] // 8) * 1024 + (r[:, None] % 8) * 128 + (((b[None, :] // 16) ^ (r[:, None] % 8)) * 16) + b[None, :] % 16
-        codes[:, kt * 128:(kt + 1) * 128] = wq[nt[:, None], kt, off]
-    scales = np.empty((N, KP // 32), dtype=np.uint8)
+        out_c[:, kt * 128:(kt + 1) * 128] = codes[nt[:, None], kt, off]
+    out_s = np.empty((tiles * rows, KT * 8), dtype=np.uint8)
     j = np.arange(8)
+    soff = (j[None, :] // 4) * 512 + (r[:, None] % 32) * 16 + (r[:, None] // 32) * 4 + j[None, :] % 4
     for kt in range(KT):
-        off = (j[None, :] // 4) * 512 + (r[:, None] % 32) * 16 + (r[:, None] // 32) * 4 + j[None, :] % 4
-        scales[:, kt * 8:(kt + 1) * 8] = ws[nt[:, None], kt, off]
-    return codes, scales
+        out_s[:, kt * 8:(kt + 1) * 8] = scales[nt[:, None], kt, soff]
+    return out_c, out_s
+
+
+def unshuffle_weight(wq, ws, N, K):
+    """Preshuffled weights (include/a4w4.h) -> plain packed codes [N, KP/2] and
+    E8M0 scales [N, KP/32] (KP = K rounded up to 256)."""
+    KT = -(-K // 256)
+    return unshuffle_tiles(wq, ws, 128, N // 128, KT)
 
 
 def gemm_violations(c_bits, ref, abs_sum):

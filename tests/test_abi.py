@@ -18,18 +18,27 @@ def L():
     return a4w4.lib()
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "a4w4.h")).read()
+def declared_functions(header="a4w4.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(a4w4_\w+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported_and_bound(L):
     names = declared_functions()
-    assert len(names) >= 17
+    assert len(names) >= 18
     for n in names:
         assert hasattr(L, n), n
         assert n in a4w4.SIGNATURES, n
+    # every binding is declared: nothing is bound that the header does not promise
+    assert sorted(a4w4.SIGNATURES) == names
+
+
+def test_debug_hooks_are_exported_and_bound(L):
+    names = declared_functions("a4w4_debug.h")
+    assert names == sorted(a4w4.DEBUG_SIGNATURES)
+    for n in names:
+        assert hasattr(L, n), n
 
 
 def test_size_functions():
@@ -81,6 +90,19 @@ def test_argument_errors_need_no_device():
     with pytest.raises(a4w4.A4W4Error) as e:
         a4w4.a4w4_moe_sort(16, 4, 2, 8, 48, 16, 16, 16, 16, 1 << 20, stream=0)   # block_m
     assert e.value.code == a4w4.A4W4_ERR_ARG
+
+
+def test_gemm_ex_rejects_unknown_flags():
+    with pytest.raises(a4w4.A4W4Error) as e:
+        a4w4.a4w4_gemm_ex(16, 1, 256, 16, 16, 256, 16, flags=2, stream=0)
+    assert e.value.code == a4w4.A4W4_ERR_ARG
+
+
+def test_debug_activation_layout_follows_the_plan():
+    assert a4w4.a4w4_debug_gemm_activation_layout(1, 7168, 4224) == (16, 1, 17)
+    assert a4w4.a4w4_debug_gemm_activation_layout(32, 7168, 4224) == (32, 1, 17)
+    assert a4w4.a4w4_debug_gemm_activation_layout(37, 1536, 4224) == (64, 1, 17)
+    assert a4w4.a4w4_debug_gemm_activation_layout(2047, 1536, 4224) == (128, 16, 17)
 
 
 def test_strerror():
