@@ -18,8 +18,11 @@ Sources (web pages, cited by title and section):
   M-tail masking; ceil-based scale accounting), Scope (N % 256 == 0,
   K % 128 == 0), Kernel microbenchmark (relative L2 2.42%-4.15%).
 * "[gfx1250] Fuse A4W4 stage1 FP4 quantization" -- Summary (MoE GEMM1
-  epilogue that emits MXFP4 codes and E8M0 scales after the SwiGLU
+  epilogue that emits MXFP4 codes and E8M0 scales after the SiLU or SwiGLU
   activation, scale taken from the FP32 activation).
+* "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4" --
+  Summary (auxiliary sort of routed rows; stage-2 paths that consume stage
+  1's output layout) and GEMM2 scope.
 * The block-scale rule itself is not stated on the pages.  The oracle uses the
   OCP Microscaling Formats (MX) v1.0 rule: shared exponent
   floor(log2(amax)) - 2 over 32 elements, clamped to the E8M0 range; E2M1
@@ -28,7 +31,8 @@ Sources (web pages, cited by title and section):
 Modules:
   mxfp4  -- E2M1/E8M0 format, block quantiser, packing, BF16 rounding
   gemm   -- the dense A4W4 GEMM (exact products, fp64 sums, BF16 output)
-  moe    -- routed-row sort and the grouped GEMM1 + SwiGLU + MXFP4 requant
+  moe    -- routed-row sort, the grouped GEMM1 + SwiGLU (or SiLU) + MXFP4
+            requant, and GEMM2 (down projection, top-k weighted sum)
 
 Parity status of every function is pinned by ``tests/test_oracle_*.py``
 (-m "not gpu"); none is "parity unpinned".

@@ -18,11 +18,25 @@ Readings (the pages leave these open):
 * W1[e] is [2I, D]: rows 0..I-1 are the gate projection, rows I..2I-1 the up
   projection; SwiGLU h = silu(gate) * up with silu(g) = g / (1 + exp(-g)), no
   clamp, no bias, top-k weights not applied in GEMM1;
+* the gfx1250 page's Summary lists SiLU beside SwiGLU as a separate epilogue
+  activation: read as the ungated form, W1[e] is [I, D] (one projection) and
+  h = silu(x . w);
 * h is requantised with the same MXFP4 rule as the inputs (oracle.mxfp4),
   once, from the float64 value (the gfx1250 page rounds to BF16 first; this
   library rounds once, from fp32);
 * output row r of the codes [T*topk, I/2] and scales [T*topk, I/32] (plain
   row-major) belongs to routed row r.
+
+GEMM2 (the down projection; "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1
+replacement to A4W4", Summary: the stage-2 paths consume stage 1's layout;
+GEMM2 scope; the pages print no formula for it).  Reading: routed row r =
+t*topk + k holds GEMM1's MXFP4 output a~_r (I values); W2[e] is [D, I]; the
+top-k weight w[t, k] that GEMM1 did not apply is applied here, and the rows
+of a token are summed:
+
+    y[t] = sum_k  w[t, k] * (W2q[topk_ids[t, k]] @ a~_{t*topk+k})      (float64)
+
+with W2q the MXFP4 quantisation of W2 (same rule), output BF16 [T, D].
 """
 
 import numpy as np
@@ -57,20 +71,24 @@ def silu(g):
         return g / (1.0 + np.exp(-g))
 
 
-def gemm1_rows(X_bits, topk_ids, expert_weight_bits, rows, inter_dim):
-    """Oracle GEMM1 + SwiGLU + requant for the routed rows ``rows``.
+def gemm1_rows(X_bits, topk_ids, expert_weight_bits, rows, inter_dim, activation="swiglu"):
+    """Oracle GEMM1 + activation + requant for the routed rows ``rows``.
 
-    X_bits [T, D] BF16 bits; expert_weight_bits(e) -> BF16 bits [2I, D].
-    Returns a dict of float64 gate/up/h (and their |.| sums) [R, I] plus the
-    expected packed codes uint8 [R, I/2] and E8M0 scales uint8 [R, I/32].
+    X_bits [T, D] BF16 bits; expert_weight_bits(e) -> BF16 bits of W1[e]:
+    [2I, D] for activation "swiglu" (h = silu(gate) * up), [I, D] for "silu"
+    (h = silu(gate)).  Returns a dict of float64 gate (and up) and their |.|
+    sums [R, I], h [R, I], the expected packed codes uint8 [R, I/2] and E8M0
+    scales uint8 [R, I/32].
     """
+    assert activation in ("swiglu", "silu")
     ids = np.asarray(topk_ids, dtype=np.int64)
     topk = ids.shape[1]
     rows = np.asarray(rows, dtype=np.int64)
     I = inter_dim
     x = {}
     wq = {}
-    out = {k: np.empty((rows.size, I)) for k in ("gate", "up", "gate_abs", "up_abs")}
+    keys = ("gate", "up", "gate_abs", "up_abs") if activation == "swiglu" else ("gate", "gate_abs")
+    out = {k: np.empty((rows.size, I)) for k in keys}
     for i, r in enumerate(rows):
         t, k = divmod(int(r), topk)
         e = int(ids[t, k])
@@ -80,13 +98,45 @@ def gemm1_rows(X_bits, topk_ids, expert_weight_bits, rows, inter_dim):
             wq[e] = mxfp4.quant_dequant(mxfp4.bf16_bits_to_f64(expert_weight_bits(e)))
         w = wq[e]
         out["gate"][i] = w[:I] @ x[t]
-        out["up"][i] = w[I:] @ x[t]
         out["gate_abs"][i] = np.abs(w[:I]) @ np.abs(x[t])
-        out["up_abs"][i] = np.abs(w[I:]) @ np.abs(x[t])
-    h = silu(out["gate"]) * out["up"]
+        if activation == "swiglu":
+            out["up"][i] = w[I:] @ x[t]
+            out["up_abs"][i] = np.abs(w[I:]) @ np.abs(x[t])
+    h = silu(out["gate"]) * out["up"] if activation == "swiglu" else silu(out["gate"])
     codes, e8m0 = mxfp4.quantize_blocks(h)
     out.update(h=h, codes=mxfp4.pack_codes(codes), scales=e8m0)
     return out
+
+
+def gemm2_tokens(a_codes, a_scales, topk_ids, topk_weights, expert_weight_bits, tokens):
+    """Oracle MoE GEMM2 (down projection + top-k weighted sum) for ``tokens``.
+
+    a_codes uint8 [T*topk, I/2] packed MXFP4 codes and a_scales uint8
+    [T*topk, I/32] E8M0 scales of every routed row (GEMM1's output, plain
+    row-major); topk_weights float32 [T, topk]; expert_weight_bits(e) -> BF16
+    bits [D, I] of W2[e].  Returns (y float64 [n, D], abs_sum float64 [n, D]
+    = sum_k |w| * sum_i |a~_i w2_i|, y rounded to BF16 bits uint16 [n, D]).
+    """
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    topk = ids.shape[1]
+    wts = np.asarray(topk_weights, dtype=np.float32).astype(np.float64)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    w2 = {}
+    y = None
+    for i, t in enumerate(tokens):
+        for k in range(topk):
+            r = int(t) * topk + k
+            e = int(ids[t, k])
+            if e not in w2:
+                w2[e] = mxfp4.quant_dequant(mxfp4.bf16_bits_to_f64(expert_weight_bits(e)))
+            a = mxfp4.decode(mxfp4.unpack_codes(a_codes[r]), a_scales[r])
+            if y is None:
+                D = w2[e].shape[0]
+                y = np.zeros((tokens.size, D))
+                abs_sum = np.zeros((tokens.size, D))
+            y[i] += wts[t, k] * (w2[e] @ a)
+            abs_sum[i] += abs(wts[t, k]) * (np.abs(w2[e]) @ np.abs(a))
+    return y, abs_sum, mxfp4.round_to_bf16_bits(y)
 
 
 def requant_fragile_blocks(h, delta):

@@ -28,7 +28,7 @@ W_STD = 0.02
 OUTLIER_FRACTION = 0.01
 OUTLIER_GAIN = 20.0
 
-_TAG_A, _TAG_W, _TAG_X, _TAG_W1, _TAG_STRESS = 11, 12, 13, 14, 15
+_TAG_A, _TAG_W, _TAG_X, _TAG_W1, _TAG_STRESS, _TAG_W2, _TAG_GATE, _TAG_H = 11, 12, 13, 14, 15, 16, 17, 18
 
 
 def rng(*key):
@@ -135,3 +135,23 @@ def moe_tokens_bits(T, D, seed=0):
 def moe_expert_weight_bits(e, two_I, D, seed=0):
     """W1[e] [2I, D] ~ N(0, 0.02) as BF16; each expert has its own stream."""
     return normal_bits((two_I, D), W_STD, seed, _TAG_W1, e, two_I, D)
+
+
+def moe_expert_w2_bits(e, D, I, seed=0):
+    """W2[e] [D, I] (down projection) ~ N(0, 0.02) as BF16; one stream per expert."""
+    return normal_bits((D, I), W_STD, seed, _TAG_W2, e, D, I)
+
+
+def moe_topk_weights(T, topk, seed=4):
+    """Routing weights float32 [T, topk]: a softmax over each token's topk
+    N(0, 1) logits (positive, each row sums to about 1)."""
+    z = rng(seed, _TAG_GATE, T, topk).standard_normal((T, topk))
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    return (p / p.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
+def moe_hidden_bits(R, I, seed=5):
+    """Stand-in GEMM1 activations [R, I] as BF16: products of two N(0, 1)
+    draws (the shape of silu(gate) * up), for feeding GEMM2 on its own."""
+    g = rng(seed, _TAG_H, R, I)
+    return to_bf16_bits((g.standard_normal((R, I)) * g.standard_normal((R, I))).astype(np.float32))
