@@ -73,7 +73,7 @@ PAGES_US = {(7168, 4224, 1): 15.960, (7168, 4224, 8): 23.041, (7168, 4224, 32): 
 # "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Performance (gfx1250, fused
 # GEMM1 operator latency in us by token count; SiTUv2 there, SwiGLU here)
 PAGES_MOE_US = {1: 47.39, 16: 201.41, 256: 676.86, 4096: 1351.28}
-ALL_WORKLOADS = ["decode", "large", "stress", "moe"]
+ALL_WORKLOADS = ["decode", "large", "stress", "moe", "moe2"]
 
 WORKLOADS = {
     "decode": ("decode-size dense A4W4 sweep, M in {1,8,32} x (N,K) in {(7168,4224),(1536,7168),(7168,768)}",
@@ -84,6 +84,8 @@ WORKLOADS = {
     "stress": ("tail/scale-edge stress, M in {37,513,2047}, N=1536, K=4224", workloads.TAIL_STRESS, "stress"),
     "moe": ("grouped MoE GEMM1 A4W4 + SwiGLU + MXFP4 requant, T in {1,16,256,4096}, E=896, topk=16, D=3584, I=768",
             [], "moe"),
+    "moe2": ("grouped MoE GEMM2 A4W4 (down projection of GEMM1's MXFP4 tiles, top-k weighted per-token sum), "
+             "T in {1,16,256,4096}, E=896, topk=16, D=3584, I=768", [], "moe2"),
 }
 
 
@@ -377,6 +379,115 @@ class MoeSweep:
         return {"T": self.items[i]["T"], "E": self.E, "topk": self.topk, "D": self.D, "I": self.I}
 
 
+class Moe2Sweep:
+    """Grouped MoE GEMM2 workload: for each token count T, the routed-row
+    sort, then GEMM2 (down projection of GEMM1's sorted-slot MXFP4 tiles
+    against W2[e] [D, I], top-k weighted fp32 rows) and the per-token sum to
+    BF16 Y [T, D] (E=896, topk=16, D=3584, I=768).  The input tiles are
+    random MXFP4 codes with E8M0 scales near 2^-7 (values do not change the
+    work); W2 ~ N(0, 0.02) as in the recipe."""
+
+    def __init__(self, dev, tokens=None):
+        import torch
+        import mxfp4_a4w4_gemm_gb300 as a4w4
+        from mxfp4_a4w4_gemm_gb300.host_prep import prepare_dense_experts_from_host
+        self.torch, self.a4w4, self.dev = torch, a4w4, dev
+        c = workloads.MOE
+        self.E, self.topk, self.D, self.I = c["experts"], c["topk"], c["model_dim"], c["inter_dim"]
+        self.tokens = list(tokens or c["tokens"])
+        self.W2q, self.W2s = prepare_dense_experts_from_host(
+            lambda e: workloads.moe_expert_w2_bits(e, self.D, self.I), self.E, self.D, self.I, threads=16, device=dev)
+        self.copies = 8
+        self.items = []
+        g = torch.Generator(device=dev)
+        g.manual_seed(6)
+        for T in self.tokens:
+            routes = []
+            maxb = a4w4.a4w4_moe_max_blocks(T, self.topk, self.E, 128)
+            for v in range(self.copies):
+                ids = workloads.moe_topk_ids(T, self.E, self.topk, seed=2 + 1000 * v)
+                wsb = a4w4.a4w4_moe_sort_workspace_bytes(T, self.topk, self.E)
+                routes.append(dict(
+                    ids=torch.from_numpy(ids).to(dev), hits=int(np.unique(ids).size),
+                    rows=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
+                    bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
+                    nb=torch.empty(1, dtype=torch.int32, device=dev),
+                    ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
+            cb = a4w4.a4w4_moe_tiles_codes_bytes(T, self.topk, self.E, self.I)
+            sb = a4w4.a4w4_moe_tiles_scales_bytes(T, self.topk, self.E, self.I)
+            aq = torch.randint(0, 256, (cb,), dtype=torch.uint8, device=dev, generator=g)
+            as_ = torch.randint(118, 124, (sb,), dtype=torch.uint8, device=dev, generator=g)
+            wts = torch.from_numpy(workloads.moe_topk_weights(T, self.topk))
+            # inputs (tiles + routing weights) in one buffer per I/O slot
+            inp_host = torch.cat([aq.cpu(), as_.cpu(), wts.view(torch.uint8).reshape(-1)])
+            wsb2 = a4w4.a4w4_moe_gemm2_workspace_bytes(T, self.topk, self.D)
+            self.items.append(dict(
+                T=T, routes=routes, cb=cb, sb=sb,
+                inp=[inp_host.to(dev) for _ in range(2)], inp_host=[inp_host.pin_memory() for _ in range(2)],
+                ws=torch.empty(wsb2, dtype=torch.uint8, device=dev), wsb=wsb2,
+                Y=[torch.empty((T, self.D), dtype=torch.bfloat16, device=dev) for _ in range(2)],
+                Y_host=[torch.empty((T, self.D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]))
+            del aq, as_
+        self.slot = 0
+        self.flags = 0
+        self.shapes = [(it["T"], self.D, self.I) for it in self.items]
+        # 3 sort kernels + GEMM2 + the per-token sum per T
+        self.launches_per_step = 5 * len(self.items)
+        self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
+        self.flops_per_step = sum(2 * it["T"] * self.topk * self.D * self.I for it in self.items)
+        torch.cuda.synchronize()
+
+    def item_bytes(self, i, r):
+        it = self.items[i]
+        T, hits = it["T"], it["routes"][r % self.copies]["hits"]
+        return int(hits * self.D * self.I * (1 / 2 + 1 / 32) + T * self.topk * self.I * (1 / 2 + 1 / 32)
+                   + 2 * T * self.D + 4 * T * self.topk)
+
+    def call(self, i, r, sort=True, gemm=True):
+        it = self.items[i]
+        ro = it["routes"][(r * len(self.items) + i) % self.copies]
+        T = it["T"]
+        if sort:
+            self.a4w4.a4w4_moe_sort(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
+                                    ro["ws"], ro["wsb"])
+        if gemm:
+            b = self.slot
+            base = it["inp"][b].data_ptr()
+            self.a4w4.a4w4_moe_gemm2(base, base + it["cb"], T, self.I, ro["rows"], ro["bexp"], ro["nb"], self.topk,
+                                     base + it["cb"] + it["sb"], self.W2q, self.W2s, self.E, self.D, it["Y"][b],
+                                     it["ws"], it["wsb"])
+
+    def step(self, r):
+        for i in range(len(self.items)):
+            self.call(i, r)
+
+    def h2d(self, b):
+        for it in self.items:
+            it["inp"][b].copy_(it["inp_host"][b], non_blocking=True)
+
+    def d2h(self, b):
+        for it in self.items:
+            it["Y_host"][b].copy_(it["Y"][b], non_blocking=True)
+
+    @property
+    def h2d_bytes(self):
+        return sum(it["inp"][0].numel() for it in self.items)
+
+    @property
+    def d2h_bytes(self):
+        return sum(2 * it["T"] * self.D for it in self.items)
+
+    def kernel_name(self, i):
+        return "a4w4_gemm_kernel<moe2,128>"
+
+    def launches_of(self, i):
+        """GEMM2 and the per-token sum."""
+        return 2
+
+    def label(self, i):
+        return {"T": self.items[i]["T"], "E": self.E, "topk": self.topk, "D": self.D, "I": self.I}
+
+
 def capture_graphs(torch, n, fn):
     graphs = []
     for r in range(n):
@@ -397,6 +508,8 @@ def make_workload(name, args, dev):
     desc, shapes, family = WORKLOADS[name]
     if name == "moe":
         return desc, MoeSweep(dev, inline=args.moe_inline)
+    if name == "moe2":
+        return desc, Moe2Sweep(dev)
     if args.shape and args.workload != "all":
         shapes = [tuple(int(v) for v in args.shape.split(","))]
         desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({name} inputs)"
@@ -430,7 +543,7 @@ def measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, pea
     durations (roofline), end-to-end with host buffers (graph-pipelined and
     eager).  Returns the workload's result block."""
     nrot = wl.copies
-    is_moe = isinstance(wl, MoeSweep)
+    is_moe = isinstance(wl, (MoeSweep, Moe2Sweep))
     # warm the library's per-device set-up before any capture, then capture
     for r in range(2):
         wl.step(r)
@@ -479,7 +592,7 @@ def measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, pea
         if is_moe:
             nbytes = sum(wl.item_bytes(i, rr) for rr in range(nrot)) / nrot
             nflops = 2 * M * wl.topk * N * K
-            pages = PAGES_MOE_US.get(M)
+            pages = PAGES_MOE_US.get(M) if name == "moe" else None
         else:
             nbytes, nflops = gemm_bytes(M, N, K), gemm_flops(M, N, K)
             pages = PAGES_US.get((N, K, M))
@@ -749,6 +862,26 @@ def oracle_moe_sample(r, rows_per_t=1):
     return done
 
 
+def oracle_moe2_sample(r):
+    """One bounded oracle step of the MoE GEMM2 workload: one token of token
+    count T (T and the token rotate with r) through the oracle's GEMM2: its
+    topk routed rows, each expert's W2 quantised in full.  Returns the
+    algorithmic bytes of the sample."""
+    from oracle import moe, mxfp4
+    c = workloads.MOE
+    E, topk, D, I = c["experts"], c["topk"], c["model_dim"], c["inter_dim"]
+    T = c["tokens"][r % len(c["tokens"])]
+    key = ("moe2", T)
+    if key not in _MOE_CACHE:
+        _MOE_CACHE[key] = (workloads.moe_hidden_bits(T * topk, I), workloads.moe_topk_ids(T, E, topk),
+                           workloads.moe_topk_weights(T, topk))
+    H, ids, wts = _MOE_CACHE[key]
+    t = (r * 7919) % T
+    q, s = mxfp4.mxfp4_quant(H[t * topk:(t + 1) * topk])
+    moe.gemm2_tokens(q, s, ids[t:t + 1], wts[t:t + 1], lambda e: workloads.moe_expert_w2_bits(e, D, I), [0])
+    return int(topk * (D * I * (1 / 2 + 1 / 32) + I * (1 / 2 + 1 / 32) + 4) + 2 * D)
+
+
 _PROBLEMS = {}
 
 
@@ -791,6 +924,10 @@ def cpu_baseline(workload, budget_s=15.0):
         step, quant = oracle_moe_sample, None
         sample = ("every token count's routed row per step through GEMM1 + SwiGLU + requant "
                   "(each row's expert quantised in full)")
+    elif workload == "moe2":
+        step, quant = oracle_moe2_sample, None
+        sample = ("one token per step (token counts 1, 16, 256, 4096 in turn) through GEMM2: its 16 routed "
+                  "rows, each expert's W2 quantised in full")
     else:
         desc, shapes, family = WORKLOADS[workload]
         for M, N, K in shapes:
@@ -833,6 +970,9 @@ def run_reference(args, rank, world):
     if name == "moe":
         step = oracle_moe_sample
         sample = "every token count's routed row per step through the oracle's GEMM1 + SwiGLU + requant"
+    elif name == "moe2":
+        step = oracle_moe2_sample
+        sample = "one token per step (token counts in turn) through the oracle's GEMM2"
     else:
         for M, N, K in shapes:
             _cached_problem(M, N, K, family)

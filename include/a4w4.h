@@ -177,6 +177,60 @@ int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
                    const void* W1q, const void* W1s, int E, int I, void* out_q, void* out_s,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* GEMM1 with a choice of activation and output layout; a4w4_moe_gemm1(...) is
+ * a4w4_moe_gemm1_ex(..., A4W4_MOE_ACT_SWIGLU, A4W4_MOE_OUT_ROWS, ...).
+ * "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Summary: the epilogue emits
+ * packed MXFP4 payloads and preshuffled E8M0 scales after SiLU or SwiGLU.
+ *   activation:
+ *     A4W4_MOE_ACT_SWIGLU  W1 prepared by a4w4_moe_prepare_w1 from [E, 2I, D]
+ *                          (gate rows then up rows); h = silu(gate) * up.
+ *     A4W4_MOE_ACT_SILU    the ungated form: W1[e] is [I, D], prepared as one
+ *                          dense matrix [E*I, D] by a4w4_prepare_gemm_weight
+ *                          (expert e starts at e * a4w4_weight_codes_bytes(I, D)
+ *                          in W1q, e * a4w4_weight_scales_bytes(I, D) in W1s);
+ *                          h = silu(x . w).  I % 256 == 0.
+ *   out_layout:
+ *     A4W4_MOE_OUT_ROWS    out_q [T*topk, I/2], out_s [T*topk, I/32], row r =
+ *                          routed row r (as a4w4_moe_gemm1).
+ *     A4W4_MOE_OUT_TILES   the operand layout a4w4_moe_gemm2 reads: for sorted
+ *                          block b (128 slots) and K tile kt (256 of the I
+ *                          columns; KT = I/256), atom a = b*KT + kt holds the
+ *                          codes of slot b*128 + r at out_q + a*16384 in the Wq
+ *                          tile layout above (row r, byte b') and its E8M0 scales
+ *                          at out_s + a*1024 in the Ws layout; padding slots
+ *                          hold zeros.  Sizes a4w4_moe_tiles_codes_bytes /
+ *                          _scales_bytes; tiles of blocks at or beyond
+ *                          *num_blocks are not written.  I % 256 == 0. */
+enum { A4W4_MOE_ACT_SWIGLU = 0, A4W4_MOE_ACT_SILU = 1 };
+enum { A4W4_MOE_OUT_ROWS = 0, A4W4_MOE_OUT_TILES = 1 };
+size_t a4w4_moe_tiles_codes_bytes(int T, int topk, int E, int I);
+size_t a4w4_moe_tiles_scales_bytes(int T, int topk, int E, int I);
+int a4w4_moe_gemm1_ex(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
+                      const int32_t* block_expert, const int32_t* num_blocks, int topk,
+                      const void* W1q, const void* W1s, int E, int I, int activation, int out_layout,
+                      void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped MoE GEMM2 (down projection) with the top-k weighted per-token sum.
+ * "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4",
+ * Summary (stage-2 paths that consume stage 1's layout) and GEMM2 scope.
+ *   Y[t, :] = sum_k topk_weights[t, k] * MXFP4(W2[e_tk]) . a~_(t*topk+k)
+ * with a~ GEMM1's MXFP4 output in A4W4_MOE_OUT_TILES layout (A_q, A_s; I
+ * columns), the same sort as GEMM1 (sorted_rows, block_expert, num_blocks,
+ * block_m 128), topk_weights float32 [T, topk] (4-byte aligned), W2q/W2s the
+ * dense preshuffled layout of the stacked [E*D, I] matrix
+ * (a4w4_prepare_gemm_weight; expert e at e * a4w4_weight_codes_bytes(D, I) and
+ * e * a4w4_weight_scales_bytes(D, I)), Y_bf16 [T, D].
+ * Each routed row's product is scaled by its weight in fp32 and stored as an
+ * fp32 row of the workspace ([T*topk, D], a4w4_moe_gemm2_workspace_bytes);
+ * a second kernel adds a token's rows in k order (bitwise deterministic) and
+ * rounds to BF16.  I % 256 == 0, D % 256 == 0. */
+size_t a4w4_moe_gemm2_workspace_bytes(int T, int topk, int D);
+int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t* sorted_rows,
+                   const int32_t* block_expert, const int32_t* num_blocks, int topk,
+                   const float* topk_weights, const void* W2q, const void* W2s, int E, int D,
+                   void* Y_bf16, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Dense A4W4 GEMM that allocates nothing (no counterpart on the source pages:
  * it exists for callers of this library).  Same arguments and result as

@@ -9,6 +9,10 @@ device memory and streams.  Build the library with
 
 from ._native import (  # noqa: F401
     A4W4_GEMM_WEIGHT_PREFETCH,
+    A4W4_MOE_ACT_SILU,
+    A4W4_MOE_ACT_SWIGLU,
+    A4W4_MOE_OUT_ROWS,
+    A4W4_MOE_OUT_TILES,
     A4W4Error,
     DEBUG_SIGNATURES,
     LIB_PATH,
@@ -23,11 +27,16 @@ from ._native import (  # noqa: F401
     a4w4_gemm_workspace_bytes,
     a4w4_get_device_status,
     a4w4_moe_gemm1,
+    a4w4_moe_gemm1_ex,
     a4w4_moe_gemm1_workspace_bytes,
+    a4w4_moe_gemm2,
+    a4w4_moe_gemm2_workspace_bytes,
     a4w4_moe_max_blocks,
     a4w4_moe_prepare_w1,
     a4w4_moe_sort,
     a4w4_moe_sort_workspace_bytes,
+    a4w4_moe_tiles_codes_bytes,
+    a4w4_moe_tiles_scales_bytes,
     a4w4_moe_w1_codes_bytes,
     a4w4_moe_w1_scales_bytes,
     a4w4_mxfp4_quant,

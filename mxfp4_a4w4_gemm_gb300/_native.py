@@ -36,6 +36,13 @@ SIGNATURES = {
     "a4w4_moe_gemm1_workspace_bytes": (_c_size, [_c_int, _c_int]),
     "a4w4_moe_gemm1": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
                                 _vp, _vp, _vp, _c_size, _vp]),
+    "a4w4_moe_tiles_codes_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "a4w4_moe_tiles_scales_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "a4w4_moe_gemm1_ex": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
+                                   _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
+    "a4w4_moe_gemm2_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_moe_gemm2": (_c_int, [_vp, _vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _vp, _c_int,
+                                _c_int, _vp, _vp, _c_size, _vp]),
     "a4w4_gemm_noalloc": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp]),
     "a4w4_get_device_status": (_c_int, [_vp]),
     "a4w4_strerror": (ctypes.c_char_p, [_c_int]),
@@ -52,6 +59,8 @@ DEBUG_SIGNATURES = {
 }
 
 A4W4_GEMM_WEIGHT_PREFETCH = 1
+A4W4_MOE_ACT_SWIGLU, A4W4_MOE_ACT_SILU = 0, 1
+A4W4_MOE_OUT_ROWS, A4W4_MOE_OUT_TILES = 0, 1
 
 _lib = None
 
@@ -185,6 +194,33 @@ def a4w4_moe_gemm1(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1
     _check("a4w4_moe_gemm1", lib().a4w4_moe_gemm1(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert),
                                                   _ptr(num_blocks), topk, _ptr(W1q), _ptr(W1s), E, I,
                                                   _ptr(out_q), _ptr(out_s), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def a4w4_moe_tiles_codes_bytes(T, topk, E, I):
+    return lib().a4w4_moe_tiles_codes_bytes(T, topk, E, I)
+
+
+def a4w4_moe_tiles_scales_bytes(T, topk, E, I):
+    return lib().a4w4_moe_tiles_scales_bytes(T, topk, E, I)
+
+
+def a4w4_moe_gemm1_ex(X, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, activation, out_layout,
+                      out_q, out_s, ws=None, ws_bytes=0, stream=None):
+    _check("a4w4_moe_gemm1_ex", lib().a4w4_moe_gemm1_ex(_ptr(X), T, D, _ptr(sorted_rows), _ptr(block_expert),
+                                                        _ptr(num_blocks), topk, _ptr(W1q), _ptr(W1s), E, I,
+                                                        activation, out_layout, _ptr(out_q), _ptr(out_s), _ptr(ws),
+                                                        ws_bytes, _stream(stream)))
+
+
+def a4w4_moe_gemm2_workspace_bytes(T, topk, D):
+    return lib().a4w4_moe_gemm2_workspace_bytes(T, topk, D)
+
+
+def a4w4_moe_gemm2(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, topk, topk_weights, W2q, W2s, E, D, Y,
+                   ws, ws_bytes, stream=None):
+    _check("a4w4_moe_gemm2", lib().a4w4_moe_gemm2(_ptr(A_q), _ptr(A_s), T, I, _ptr(sorted_rows), _ptr(block_expert),
+                                                  _ptr(num_blocks), topk, _ptr(topk_weights), _ptr(W2q), _ptr(W2s),
+                                                  E, D, _ptr(Y), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def a4w4_gemm_noalloc(A, M, K, Wq, Ws, N, C, stream=None):

@@ -98,9 +98,14 @@ int gemm_impl(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, 
 }
 
 int moe_gemm1_impl(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
-                   const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
-                   void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream, a4w4::ActDump dump) {
+                   const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I, int act,
+                   int out_layout, void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream,
+                   a4w4::ActDump dump) {
   if (T <= 0 || D <= 0 || topk <= 0 || E <= 0 || I <= 0 || I % 128 != 0 || D % 128 != 0) return A4W4_ERR_ARG;
+  if (act != A4W4_MOE_ACT_SWIGLU && act != A4W4_MOE_ACT_SILU) return A4W4_ERR_ARG;
+  if (out_layout != A4W4_MOE_OUT_ROWS && out_layout != A4W4_MOE_OUT_TILES) return A4W4_ERR_ARG;
+  // SiLU tiles hold 256 output columns; operand tiles are whole 256-wide K tiles
+  if ((act == A4W4_MOE_ACT_SILU || out_layout == A4W4_MOE_OUT_TILES) && I % 256 != 0) return A4W4_ERR_ARG;
   if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
   if (!aligned16(X_bf16) || !aligned16(W1q) || !aligned16(W1s) || !aligned16(out_q) || out_s == nullptr ||
       sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr)
@@ -117,8 +122,8 @@ int moe_gemm1_impl(const void* X_bf16, int T, int D, const int32_t* sorted_rows,
     xq = ws;
   }
   return a4w4::launch_moe_gemm1(X_bf16, T, D, sorted_rows, block_expert, num_blocks, max_blocks, topk, W1q, W1s,
-                                E, I, out_q, out_s, xq, as_stream(stream), g_wait_ns.load(std::memory_order_relaxed),
-                                status, sms, dump);
+                                E, I, act, out_layout == A4W4_MOE_OUT_TILES ? 1 : 0, out_q, out_s, xq,
+                                as_stream(stream), g_wait_ns.load(std::memory_order_relaxed), status, sms, dump);
 }
 
 }  // namespace
@@ -236,8 +241,57 @@ size_t a4w4_moe_gemm1_workspace_bytes(int T, int D) {
 int a4w4_moe_gemm1(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                    const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
                    void* out_q, void* out_s, void* ws, size_t ws_bytes, void* stream) {
-  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
-                        ws, ws_bytes, stream, a4w4::ActDump{});
+  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I,
+                        A4W4_MOE_ACT_SWIGLU, A4W4_MOE_OUT_ROWS, out_q, out_s, ws, ws_bytes, stream, a4w4::ActDump{});
+}
+
+int a4w4_moe_gemm1_ex(const void* X_bf16, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
+                      const int32_t* num_blocks, int topk, const void* W1q, const void* W1s, int E, int I,
+                      int activation, int out_layout, void* out_q, void* out_s, void* ws, size_t ws_bytes,
+                      void* stream) {
+  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, activation,
+                        out_layout, out_q, out_s, ws, ws_bytes, stream, a4w4::ActDump{});
+}
+
+size_t a4w4_moe_tiles_codes_bytes(int T, int topk, int E, int I) {
+  if (T <= 0 || topk <= 0 || E <= 0 || I <= 0) return 0;
+  return static_cast<size_t>(a4w4_moe_max_blocks(T, topk, E, 128)) * ((I + 255) / 256) * 16384;
+}
+
+size_t a4w4_moe_tiles_scales_bytes(int T, int topk, int E, int I) {
+  if (T <= 0 || topk <= 0 || E <= 0 || I <= 0) return 0;
+  return static_cast<size_t>(a4w4_moe_max_blocks(T, topk, E, 128)) * ((I + 255) / 256) * 1024;
+}
+
+size_t a4w4_moe_gemm2_workspace_bytes(int T, int topk, int D) {
+  if (T <= 0 || topk <= 0 || D <= 0) return 0;
+  return static_cast<size_t>(T) * topk * D * sizeof(float);
+}
+
+int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t* sorted_rows,
+                   const int32_t* block_expert, const int32_t* num_blocks, int topk, const float* topk_weights,
+                   const void* W2q, const void* W2s, int E, int D, void* Y_bf16, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (T <= 0 || I <= 0 || topk <= 0 || E <= 0 || D <= 0 || I % 256 != 0 || D % 256 != 0) return A4W4_ERR_ARG;
+  if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
+  if (!aligned16(A_q) || A_s == nullptr || !aligned16(W2q) || !aligned16(W2s) || !aligned16(Y_bf16) ||
+      sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr || topk_weights == nullptr ||
+      (reinterpret_cast<uintptr_t>(topk_weights) & 3u) != 0)
+    return A4W4_ERR_ARG;
+  if (!aligned16(ws) || ws_bytes < a4w4_moe_gemm2_workspace_bytes(T, topk, D)) return A4W4_ERR_WORKSPACE;
+  const int sms = current_device_sms();
+  if (sms < 0) return sms;
+  const int max_blocks = a4w4_moe_max_blocks(T, topk, E, 128);
+  if (max_blocks > 65535) return A4W4_ERR_ARG;
+  unsigned int* status = status_ptr();
+  if (status == nullptr) return A4W4_ERR_LAUNCH;
+  const cudaStream_t st = as_stream(stream);
+  float* partial = static_cast<float*>(ws);
+  const int rc = a4w4::launch_moe_gemm2(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, max_blocks, topk,
+                                        topk_weights, W2q, W2s, E, D, partial, st,
+                                        g_wait_ns.load(std::memory_order_relaxed), status);
+  if (rc != 0) return rc;
+  return a4w4::launch_moe_sum(partial, T, topk, D, Y_bf16, st, sms);
 }
 
 // ---------------------------------------------------------------------------
@@ -286,8 +340,8 @@ int a4w4_debug_moe_gemm1_export(const void* X_bf16, int T, int D, const int32_t*
   if (dump_bytes < atoms * (16384 + 1024)) return A4W4_ERR_ARG;
   if (cudaMemsetAsync(dump, 0, atoms * (16384 + 1024), as_stream(stream)) != cudaSuccess) return A4W4_ERR_LAUNCH;
   a4w4::ActDump d{static_cast<uint8_t*>(dump), static_cast<uint8_t*>(dump) + atoms * 16384};
-  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I, out_q, out_s,
-                        ws, ws_bytes, stream, d);
+  return moe_gemm1_impl(X_bf16, T, D, sorted_rows, block_expert, num_blocks, topk, W1q, W1s, E, I,
+                        A4W4_MOE_ACT_SWIGLU, A4W4_MOE_OUT_ROWS, out_q, out_s, ws, ws_bytes, stream, d);
 }
 
 int a4w4_get_device_status(void* stream) {

@@ -32,8 +32,13 @@ namespace a4w4 {
 // kMoe: kNormal over gathered sorted rows with the SwiGLU +
 // requant epilogue; kPre: rows quantised beforehand into tiles, both operands
 // streamed by TMA (large M); kMoePre: kMoe gathering rows that were quantised
-// once beforehand (plain MXFP4 layout) instead of quantising them per tile.
-enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4 };
+// once beforehand (plain MXFP4 layout) instead of quantising them per tile;
+// kMoe2: MoE GEMM2, GEMM1's output tiles (sorted-slot operand layout) streamed
+// by TMA against the expert's down projection, top-k weighted fp32 rows out.
+enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4, kMoe2 = 5 };
+
+// MoE GEMM1 epilogue activation (a4w4.h: A4W4_MOE_ACT_*)
+constexpr int kActSwiglu = 0, kActSilu = 1;
 
 struct GemmArgs {
   const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
@@ -57,6 +62,10 @@ struct GemmArgs {
   long long expert_code_bytes, expert_sf_bytes;
   uint8_t* out_q;
   uint8_t* out_s;
+  int act;              // kActSwiglu or kActSilu
+  int out_tiles;        // 1: GEMM1 output in sorted-slot operand tiles (KT_out K tiles per block)
+  int KT_out;
+  const float* topk_w;  // GEMM2: routing weight of each routed row
   // test hook (ActDump): the CTAs of weight tile 0 also store the activation
   // tiles their producers build; nullptr in every product call
   uint8_t* dump_codes;
@@ -73,8 +82,9 @@ struct Cfg {
   static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
-  static constexpr bool kTmaA = MODE == kPre;                    // activations arrive by TMA too
-  static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;
+  static constexpr bool kTmaA = MODE == kPre || MODE == kMoe2;   // activations arrive by TMA too
+  static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;  // MoE GEMM1
+  static constexpr bool kRouted = kMoeAny || MODE == kMoe2;        // blocks of sorted routed rows
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
   static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer warps
   // epilogue warps (the first of the producer warps): MoE's SwiGLU + requant
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   const int split = blockIdx.z;
 
   int expert = 0;
-  if (Cf::kMoeAny) {
+  if (Cf::kRouted) {
     griddep_wait();                                // the sort that wrote num_blocks has finished
     if (x_tile >= *p.num_blocks) return;           // block does not exist for this routing
     expert = p.block_expert[x_tile];
@@ -188,14 +198,19 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   // no empty-slot wait (fresh barriers).
   const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
   const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
+  // Dense large-M tiles re-read each weight tile from L2 once per activation
+  // tile (evict-last); swap-AB and MoE GEMM1 stream every weight byte once.
+  // MoE GEMM2 reads each block's activation tiles once per output-column
+  // tile (evict-last) and the expert's weights about once (evict-first).
   const uint64_t pol = (MODE == kNormal || MODE == kPre) ? policy_evict_last() : policy_evict_first();
+  const uint64_t pol_a = Cf::kTmaA ? policy_evict_last() : pol;
   auto issue_stage = [&](int i) {
     const int s = i % STAGES;
     mbar_arrive_expect_tx(full_w(s), (Cf::W_ATOMS + (Cf::kTmaA ? 1 : 0)) * (16384 + 1024));
     if (Cf::kTmaA) {
       const long long atom = static_cast<long long>(x_tile) * p.KT + (kt0 + i);
-      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol);
-      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol);
+      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
+      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
     }
 #pragma unroll
     for (int a = 0; a < Cf::W_ATOMS; ++a) {
@@ -234,8 +249,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   if (warp == 0) {
     // ---------------- weight producer ----------------
     if (lane == 0 && nk > 0) {
-      // Dense large-M tiles re-read each weight tile from L2 once per activation
-      // tile (evict-last); swap-AB and MoE stream every weight byte once.
       int i = issued;
       for (; i < nk; ++i) {
         const int s = i % STAGES;
@@ -636,24 +649,72 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
               if (warp == 2 && lane == 0) p.counters[tile] = 0u;
             }
           }
-        } else {  // kMoe, kMoePre: SwiGLU + MXFP4 requant of 128 output columns per CTA
+        } else if (MODE == kMoe2) {
+          // MoE GEMM2: each valid sorted slot's fp32 row (256 output columns)
+          // times its routing weight, staged in the drained ring (pitch 1040
+          // bytes) and written to row `entry` of the [T*topk, D] partial
+          // buffer with one 1 KB bulk store; padding slots write nothing.
           const int entry = p.sorted_rows[x_tile * 128 + lrow];
           const bool valid = entry >= 0 && entry < p.routed_rows;
-          const int jc0 = w_tile * 128;
-          const int half = (warp - 2) >> 2;           // which 64 of the 128 output columns
+          const float wgt = valid ? __ldg(p.topk_w + entry) : 0.f;
+          constexpr int kRowPitch = 1040;
+          float* my = reinterpret_cast<float*>(smem + lrow * kRowPitch);
 #pragma unroll 1
-          for (int g4 = 2 * half; g4 < 2 * half + 2; ++g4) {
-            float g[32], u[32], h[32];
+          for (int c0 = 0; c0 < 256; c0 += 64) {
+            float v[64];
+            tmem_ld64(tq + c0, v);
+            float4* d = reinterpret_cast<float4*>(my + c0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              d[j] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1], wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          if (valid) {
+            bulk_s2g(p.partial + static_cast<long long>(entry) * p.N + w_tile * 256,
+                     base + static_cast<uint32_t>(lrow * kRowPitch), 1024);
+            bulk_commit_wait_read();
+          }
+        } else {  // kMoe, kMoePre: activation + MXFP4 requant of the CTA's output columns
+          // SwiGLU: 128 output columns per CTA (accumulator columns 0..127
+          // gate, 128..255 up); SiLU: 256 output columns, one accumulator
+          // column each.  Two warps per TMEM lane quadrant split the columns.
+          const int slot = x_tile * 128 + lrow;
+          const int entry = p.sorted_rows[slot];
+          const bool valid = entry >= 0 && entry < p.routed_rows;
+          const bool silu_only = p.act == kActSilu;
+          const int groups = silu_only ? 4 : 2;        // 32-column groups per warp
+          const int jc0 = w_tile * (silu_only ? 256 : 128);
+          const int half = (warp - 2) >> 2;
+#pragma unroll 1
+          for (int gi = 0; gi < groups; ++gi) {
+            const int g4 = groups * half + gi;
+            float g[32], h[32];
             tmem_ld16(tq + g4 * 32, g);
             tmem_ld16(tq + g4 * 32 + 16, g + 16);
-            tmem_ld16(tq + 128 + g4 * 32, u);
-            tmem_ld16(tq + 128 + g4 * 32 + 16, u + 16);
+            if (silu_only) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+              for (int i = 0; i < 32; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i]));
+            } else {
+              float u[32];
+              tmem_ld16(tq + 128 + g4 * 32, u);
+              tmem_ld16(tq + 128 + g4 * 32 + 16, u + 16);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] = __fdividef(g[i], 1.0f + __expf(-g[i])) * u[i];
+            }
             uint32_t c[4];
             const uint32_t e = quant32_f32(h, c);
-            if (valid) {
-              const int col = jc0 + g4 * 32;
+            const int col = jc0 + g4 * 32;
+            if (p.out_tiles) {
+              // sorted-slot operand tiles (GEMM2's A operand): every slot is
+              // written; a padding slot's accumulator row is zero, so are its
+              // codes and scale
+              const long long atom = static_cast<long long>(x_tile) * p.KT_out + col / 256;
+              const int j = (col % 256) / 32;
+              *reinterpret_cast<uint4*>(p.out_q + atom * 16384 + (lrow >> 3) * 1024 + (lrow & 7) * 128 +
+                                        ((j ^ (lrow & 7)) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+              p.out_s[atom * 1024 + (j >> 2) * 512 + (lrow & 31) * 16 + (lrow >> 5) * 4 + (j & 3)] =
+                  static_cast<uint8_t>(e);
+            } else if (valid) {
               *reinterpret_cast<uint4*>(p.out_q + static_cast<long long>(entry) * (p.I / 2) + col / 2) = make_uint4(c[0], c[1], c[2], c[3]);
               p.out_s[static_cast<long long>(entry) * (p.I / 32) + col / 32] = static_cast<uint8_t>(e);
             }
@@ -913,8 +974,8 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
 
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s, int E,
-                     int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st, unsigned long long wait_ns,
-                     unsigned int* status, int sms, ActDump dump) {
+                     int I, int act, int out_tiles, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
+                     unsigned long long wait_ns, unsigned int* status, int sms, ActDump dump) {
   GemmArgs a{};
   a.status = status;
   a.dump_codes = dump.codes;
@@ -922,7 +983,8 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
   a.A = static_cast<const uint16_t*>(X);
   a.Wq = static_cast<const uint8_t*>(W1q);
   a.Ws = static_cast<const uint8_t*>(W1s);
-  a.M = T; a.N = 2 * I; a.K = D; a.KT = (D + 255) / 256; a.splits = 1; a.w_tiles = I / 128;
+  const int rows = act == kActSilu ? I : 2 * I;     // weight rows per expert
+  a.M = T; a.N = rows; a.K = D; a.KT = (D + 255) / 256; a.splits = 1; a.w_tiles = rows / 256;
   a.wait_ns = wait_ns;
   a.sorted_rows = sorted_rows;
   a.block_expert = block_expert;
@@ -931,9 +993,12 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
   a.routed_rows = T * topk;
   a.I = I;
   a.E = E;
+  a.act = act;
+  a.out_tiles = out_tiles;
+  a.KT_out = (I + 255) / 256;
   const long long kp = static_cast<long long>(a.KT) * 256;
-  a.expert_code_bytes = static_cast<long long>(2 * I) * kp / 2;
-  a.expert_sf_bytes = static_cast<long long>(2 * I) * kp / 32;
+  a.expert_code_bytes = static_cast<long long>(rows) * kp / 2;
+  a.expert_sf_bytes = static_cast<long long>(rows) * kp / 32;
   a.out_q = static_cast<uint8_t*>(out_q);
   a.out_s = static_cast<uint8_t*>(out_s);
   if (max_blocks <= 0) return 0;
@@ -945,9 +1010,37 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
     if (rc != 0) return rc;
     a.Aq = xq;
     a.As = xs;
-    return launch_cfg<kMoePre, 128, 4>(a, dim3(I / 128, max_blocks, 1), st);
+    return launch_cfg<kMoePre, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
   }
-  return launch_cfg<kMoe, 128, 4>(a, dim3(I / 128, max_blocks, 1), st);
+  return launch_cfg<kMoe, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
+}
+
+int launch_moe_gemm2(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
+                     const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
+                     const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
+                     cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
+  GemmArgs a{};
+  a.status = status;
+  a.Aq = static_cast<const uint8_t*>(Aq);
+  a.As = static_cast<const uint8_t*>(As);
+  a.Wq = static_cast<const uint8_t*>(W2q);
+  a.Ws = static_cast<const uint8_t*>(W2s);
+  a.M = T; a.N = D; a.K = I; a.KT = (I + 255) / 256; a.splits = 1; a.w_tiles = D / 256;
+  a.wait_ns = wait_ns;
+  a.sorted_rows = sorted_rows;
+  a.block_expert = block_expert;
+  a.num_blocks = num_blocks;
+  a.topk = topk;
+  a.routed_rows = T * topk;
+  a.I = I;
+  a.E = E;
+  a.topk_w = topk_w;
+  a.partial = partial;
+  const long long kp = static_cast<long long>(a.KT) * 256;
+  a.expert_code_bytes = static_cast<long long>(D) * kp / 2;
+  a.expert_sf_bytes = static_cast<long long>(D) * kp / 32;
+  if (max_blocks <= 0) return 0;
+  return launch_cfg<kMoe2, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
 }
 
 }  // namespace a4w4

@@ -44,6 +44,25 @@ int ensure_func_attrs(std::atomic<unsigned long long>& done, SetFn set) {
   return 0;
 }
 
+// Launch `kern` on a 1-D grid with programmatic stream serialisation (the
+// kernels launched this way order their global reads after
+// griddepcontrol.wait, so they may start while the previous grid finishes).
+// Returns 0 or -4.
+template <typename... Params, typename... Args>
+int launch_pdl(void (*kern)(Params...), int grid, int block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return -4;
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 // Shared by the C ABI entry points (defined in api.cu): SM count of the
 // current device if it is a compute capability 10.3 GPU, else a negative
 // A4W4 error code; device address of the status word; the current wait limit.
@@ -75,10 +94,20 @@ int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* W
 int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                   void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w,
                   ActDump dump);
+// act: 0 SwiGLU (W1[e] = [2I, D] paired gate/up layout), 1 SiLU (W1[e] =
+// [I, D] dense layout); out_tiles: 1 = sorted-slot operand tiles.
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,
                      const int32_t* num_blocks, int max_blocks, int topk, const void* W1q, const void* W1s,
-                     int E, int I, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
+                     int E, int I, int act, int out_tiles, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
                      unsigned long long wait_ns, unsigned int* status, int sms, ActDump dump);
+// MoE GEMM2: GEMM1's sorted-slot tiles x W2[e] ([D, I] dense layout per
+// expert) -> top-k weighted fp32 rows partial[T*topk, D].
+int launch_moe_gemm2(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
+                     const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
+                     const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
+                     cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
+// Y[t, :] (BF16) = sum over k = 0..topk-1, in that order, of partial[t*topk + k, :].
+int launch_moe_sum(const float* partial, int T, int topk, int D, void* Y, cudaStream_t st, int sms);
 int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
                     int32_t* block_expert, int32_t* num_blocks, void* ws, cudaStream_t st);
 size_t moe_sort_ws_bytes(int T, int topk, int E);

@@ -1,4 +1,5 @@
-// moe.cu -- routed-row sort for the grouped MoE GEMM1.
+// moe.cu -- routed-row sort for the grouped MoE GEMMs, and GEMM2's per-token
+// reduction of the top-k weighted rows.
 //
 // "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4",
 // Summary: GEMM1 consumes token->expert rows grouped per expert by an auxiliary
@@ -130,6 +131,49 @@ int launch_moe_sort(const int32_t* ids, int T, int topk, int E, int bm, int32_t*
   moe_scan_kernel<<<1, 1024, 0, st>>>(hist, nchunks, E, bm, n, sorted_rows, block_expert, num_blocks);
   moe_place_kernel<<<nchunks, 32, shm, st>>>(ids, n, E, hist, sorted_rows);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// GEMM2's last step ("[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1
+// replacement to A4W4", GEMM2 scope; the down projection's rows of one token
+// are summed): Y[t, n] = sum_{k < topk} partial[t*topk + k, n], added in k
+// order in fp32 (bitwise deterministic), rounded to BF16.  One thread per 8
+// consecutive columns of a token: two 16-byte loads per routed row, one
+// 16-byte store.  HBM-bound: 4*topk bytes read and 2 written per output.
+__global__ void __launch_bounds__(256) moe_sum_kernel(const float4* __restrict__ part, int T, int topk, int D,
+                                                      uint4* __restrict__ y) {
+  griddep_wait();                 // the GEMM2 that wrote `part` has completed
+  griddep_launch_dependents();
+  const int g8 = D / 8;
+  const long long items = static_cast<long long>(T) * g8;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < items; i += stride) {
+    const long long t = i / g8;
+    const int c = static_cast<int>(i - t * g8);
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float4* src = part + (t * topk) * (D / 4) + 2 * c;
+    for (int k = 0; k < topk; ++k) {
+      const float4 u = __ldcs(src), v = __ldcs(src + 1);
+      a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+      a[4] += v.x; a[5] += v.y; a[6] += v.z; a[7] += v.w;
+      src += D / 4;
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(a[2 * j], a[2 * j + 1]);
+      o[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    y[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+int launch_moe_sum(const float* partial, int T, int topk, int D, void* Y, cudaStream_t st, int sms) {
+  const long long items = static_cast<long long>(T) * (D / 8);
+  long long grid = (items + 255) / 256;
+  if (grid > static_cast<long long>(sms) * 8) grid = static_cast<long long>(sms) * 8;
+  if (grid < 1) grid = 1;
+  return launch_pdl(moe_sum_kernel, static_cast<int>(grid), 256, st, reinterpret_cast<const float4*>(partial), T,
+                    topk, D, static_cast<uint4*>(Y));
 }
 
 }  // namespace a4w4

@@ -82,25 +82,6 @@ __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __r
   }
 }
 
-// Launch with programmatic stream serialisation (the kernels above order
-// their global reads after griddepcontrol.wait).  The one-time weight
-// preparation launches this way too but triggers its dependents only at
-// completion (see prepare_weight_kernel).
-template <typename... Params, typename... Args>
-static int launch_pdl(void (*kern)(Params...), int grid, int block, cudaStream_t st, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(block, 1, 1);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return -4;
-  return cudaGetLastError() == cudaSuccess ? 0 : -4;
-}
-
 static int grid_for(long long items, int threads, int sms, int per_sm) {
   long long g = (items + threads - 1) / threads;
   const long long cap = static_cast<long long>(sms) * per_sm;

@@ -44,6 +44,26 @@ def unshuffle_tiles(codes, scales, rows, tiles, KT):
     return out_c, out_s
 
 
+def shuffle_tiles(codes, scales, rows, tiles, KT):
+    """Inverse of unshuffle_tiles: plain packed codes [tiles*rows, KT*128] and
+    scales [tiles*rows, KT*8] -> (tile codes bytes, tile scale bytes) in the
+    header's operand layout (scale-atom rows beyond `rows` stay zero)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    out_c = np.zeros((tiles, KT, rows * 128), dtype=np.uint8)
+    out_s = np.zeros((tiles, KT, 1024), dtype=np.uint8)
+    n = np.arange(tiles * rows)
+    nt, r = n // rows, n % rows
+    b = np.arange(128)
+    off = (r[:, None] // 8) * 1024 + (r[:, None] % 8) * 128 + (((b[None, :] // 16) ^ (r[:, None] % 8)) * 16) + b[None, :] % 16
+    j = np.arange(8)
+    soff = (j[None, :] // 4) * 512 + (r[:, None] % 32) * 16 + (r[:, None] // 32) * 4 + j[None, :] % 4
+    for kt in range(KT):
+        out_c[nt[:, None], kt, off] = codes[:, kt * 128:(kt + 1) * 128]
+        out_s[nt[:, None], kt, soff] = scales[:, kt * 8:(kt + 1) * 8]
+    return out_c.reshape(-1), out_s.reshape(-1)
+
+
 def unshuffle_weight(wq, ws, N, K):
     """Preshuffled weights (include/a4w4.h) -> plain packed codes [N, KP/2] and
     E8M0 scales [N, KP/32] (KP = K rounded up to 256)."""
