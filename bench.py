@@ -275,9 +275,26 @@ class DenseSweep:
         return {"M": M, "N": N, "K": K}
 
 
+def sort_buffers(a4w4, torch, dev, ids, E, maxb):
+    """Device buffers of one routing for the single-launch sort (its
+    workspace zeroed once, as the library asks)."""
+    T, topk = ids.shape
+    wsb = a4w4.a4w4_moe_sort_aux_workspace_bytes(T, topk, E)
+    ro = dict(ids=torch.from_numpy(ids).to(dev), hits=int(np.unique(ids).size),
+              rows=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
+              toks=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
+              slot=torch.empty(T * topk, dtype=torch.int32, device=dev),
+              bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
+              nb=torch.empty(1, dtype=torch.int32, device=dev),
+              ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb)
+    a4w4.a4w4_workspace_init(ro["ws"], wsb)
+    return ro
+
+
 class MoeSweep:
     """Grouped MoE GEMM1 workload: for each token count T, the routed-row sort
-    and GEMM1 + SwiGLU + MXFP4 requant (E=896, topk=16, D=3584, I=768)."""
+    (single launch, with the gather/scatter arrays) and GEMM1 + SwiGLU + MXFP4
+    requant (E=896, topk=16, D=3584, I=768)."""
 
     def __init__(self, dev, tokens=None, inline=False):
         self.inline = inline
@@ -300,13 +317,7 @@ class MoeSweep:
             for v in range(self.copies):
                 ids = workloads.moe_topk_ids(T, self.E, self.topk, seed=2 + 1000 * v)
                 maxb = a4w4.a4w4_moe_max_blocks(T, self.topk, self.E, 128)
-                wsb = a4w4.a4w4_moe_sort_workspace_bytes(T, self.topk, self.E)
-                routes.append(dict(
-                    ids=torch.from_numpy(ids).to(dev), hits=int(np.unique(ids).size),
-                    rows=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
-                    bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
-                    nb=torch.empty(1, dtype=torch.int32, device=dev),
-                    ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
+                routes.append(sort_buffers(a4w4, torch, dev, ids, self.E, maxb))
             # quantise tokens once (workspace) unless T = 1 or inline quant is forced
             xwsb = 0 if (T == 1 or self.inline) else a4w4.a4w4_moe_gemm1_workspace_bytes(T, self.D)
             # tokens and outputs in two I/O slots (see DenseSweep); sort and
@@ -323,8 +334,8 @@ class MoeSweep:
         self.slot = 0
         self.flags = 0
         self.shapes = [(it["T"], 2 * self.I, self.D) for it in self.items]
-        # 3 sort kernels + GEMM1 per T, + the token quantisation when GEMM1 has a workspace
-        self.launches_per_step = sum(4 + (1 if it["xws"] is not None else 0) for it in self.items)
+        # the sort + GEMM1 per T, + the token quantisation when GEMM1 has a workspace
+        self.launches_per_step = sum(2 + (1 if it["xws"] is not None else 0) for it in self.items)
         self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
         self.flops_per_step = sum(2 * it["T"] * self.topk * 2 * self.I * self.D for it in self.items)
         torch.cuda.synchronize()
@@ -339,8 +350,8 @@ class MoeSweep:
         ro = it["routes"][(r * len(self.items) + i) % self.copies]
         T = it["T"]
         if sort:
-            self.a4w4.a4w4_moe_sort(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
-                                    ro["ws"], ro["wsb"])
+            self.a4w4.a4w4_moe_sort_aux(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
+                                        ro["toks"], ro["slot"], ro["ws"], ro["wsb"])
         if gemm:
             b = self.slot
             self.a4w4.a4w4_moe_gemm1(it["X"][b], T, self.D, ro["rows"], ro["bexp"], ro["nb"], self.topk,
@@ -406,13 +417,7 @@ class Moe2Sweep:
             maxb = a4w4.a4w4_moe_max_blocks(T, self.topk, self.E, 128)
             for v in range(self.copies):
                 ids = workloads.moe_topk_ids(T, self.E, self.topk, seed=2 + 1000 * v)
-                wsb = a4w4.a4w4_moe_sort_workspace_bytes(T, self.topk, self.E)
-                routes.append(dict(
-                    ids=torch.from_numpy(ids).to(dev), hits=int(np.unique(ids).size),
-                    rows=torch.empty(maxb * 128, dtype=torch.int32, device=dev),
-                    bexp=torch.empty(maxb, dtype=torch.int32, device=dev),
-                    nb=torch.empty(1, dtype=torch.int32, device=dev),
-                    ws=torch.empty(wsb, dtype=torch.uint8, device=dev), wsb=wsb))
+                routes.append(sort_buffers(a4w4, torch, dev, ids, self.E, maxb))
             cb = a4w4.a4w4_moe_tiles_codes_bytes(T, self.topk, self.E, self.I)
             sb = a4w4.a4w4_moe_tiles_scales_bytes(T, self.topk, self.E, self.I)
             aq = torch.randint(0, 256, (cb,), dtype=torch.uint8, device=dev, generator=g)
@@ -431,8 +436,8 @@ class Moe2Sweep:
         self.slot = 0
         self.flags = 0
         self.shapes = [(it["T"], self.D, self.I) for it in self.items]
-        # 3 sort kernels + GEMM2 + the per-token sum per T
-        self.launches_per_step = 5 * len(self.items)
+        # the sort + GEMM2 + the per-token sum per T
+        self.launches_per_step = 3 * len(self.items)
         self.bytes_per_step = sum(self.item_bytes(i, 0) for i in range(len(self.items)))
         self.flops_per_step = sum(2 * it["T"] * self.topk * self.D * self.I for it in self.items)
         torch.cuda.synchronize()
@@ -448,8 +453,8 @@ class Moe2Sweep:
         ro = it["routes"][(r * len(self.items) + i) % self.copies]
         T = it["T"]
         if sort:
-            self.a4w4.a4w4_moe_sort(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
-                                    ro["ws"], ro["wsb"])
+            self.a4w4.a4w4_moe_sort_aux(ro["ids"], T, self.topk, self.E, 128, ro["rows"], ro["bexp"], ro["nb"],
+                                        ro["toks"], ro["slot"], ro["ws"], ro["wsb"])
         if gemm:
             b = self.slot
             base = it["inp"][b].data_ptr()
@@ -596,7 +601,21 @@ def measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, pea
         else:
             nbytes, nflops = gemm_bytes(M, N, K), gemm_flops(M, N, K)
             pages = PAGES_US.get((N, K, M))
-        per.append(dict(wl.label(i), us=round(us, 3), tbs=round(nbytes / us / 1e6, 3),
+        extra = {}
+        if is_moe:
+            # the single-launch sort of the same routings, timed alone
+            g = capture_graphs(torch, 1, lambda _r, i=i: [wl.call(i, rr, gemm=False) for rr in range(nrot)])[0]
+            g.replay()
+            torch.cuda.synchronize()
+            s0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            s1.record(stream)
+            torch.cuda.synchronize()
+            launches += reps * nrot
+            extra["sort_us"] = round(s0.elapsed_time(s1) * 1e3 / (reps * nrot), 3)
+            del g
+        per.append(dict(wl.label(i), **extra, us=round(us, 3), tbs=round(nbytes / us / 1e6, 3),
                         tflops=round(nflops / us / 1e6, 2), kernel=wl.kernel_name(i), bytes=int(nbytes),
                         flops=int(nflops), hbm_frac=round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4),
                         fp4_frac=round(nflops / us / 1e6 / fp4_peak_tflops(peaks), 4),

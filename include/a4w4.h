@@ -159,6 +159,24 @@ int a4w4_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m,
                   int32_t* sorted_rows, int32_t* block_expert, int32_t* num_blocks,
                   void* ws, size_t ws_bytes, void* stream);
 
+/* The same sort in one launch, with the auxiliary gather/scatter arrays.
+ * "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4",
+ * Summary (the adaptive MoE auxiliary sort; its review names the aux arrays
+ * the sort emits for A4W4).  sorted_rows, block_expert and num_blocks are
+ * identical to a4w4_moe_sort's; in addition sorted_tokens[s] is the token
+ * (r / topk) of sorted slot s, or T for a padding slot (same length as
+ * sorted_rows), and row_slot[r] is the slot that holds routed row r (int32
+ * [T*topk]).  One cooperative launch of up to one CTA per SM, one CTA for up
+ * to 2048 routed rows (a decode batch).  E <= 4096, T*topk <= 32768 x the
+ * SM count.  ws >= a4w4_moe_sort_aux_workspace_bytes(T, topk, E) bytes, 16-byte
+ * aligned, zeroed once with a4w4_workspace_init (it ends with a grid barrier
+ * that resets itself; re-initialise after a TIMEOUT). */
+size_t a4w4_moe_sort_aux_workspace_bytes(int T, int topk, int E);
+int a4w4_moe_sort_aux(const int32_t* topk_ids, int T, int topk, int E, int block_m,
+                      int32_t* sorted_rows, int32_t* block_expert, int32_t* num_blocks,
+                      int32_t* sorted_tokens, int32_t* row_slot, void* ws, size_t ws_bytes,
+                      void* stream);
+
 /* GEMM1 over sorted rows (block_m must be 128).  For every routed row r listed
  * by the sort: g = MXFP4(X[t]) . MXFP4(W1[e, gate rows]), u = ... (up rows),
  * h = silu(g) * u in fp32 (silu(g) = g / (1 + exp(-g)); no clamp, no bias,

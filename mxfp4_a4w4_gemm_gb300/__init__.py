@@ -34,6 +34,8 @@ from ._native import (  # noqa: F401
     a4w4_moe_max_blocks,
     a4w4_moe_prepare_w1,
     a4w4_moe_sort,
+    a4w4_moe_sort_aux,
+    a4w4_moe_sort_aux_workspace_bytes,
     a4w4_moe_sort_workspace_bytes,
     a4w4_moe_tiles_codes_bytes,
     a4w4_moe_tiles_scales_bytes,

@@ -33,6 +33,9 @@ SIGNATURES = {
     "a4w4_moe_max_blocks": (_c_int, [_c_int, _c_int, _c_int, _c_int]),
     "a4w4_moe_sort_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "a4w4_moe_sort": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _i32p, _vp, _c_size, _vp]),
+    "a4w4_moe_sort_aux_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int]),
+    "a4w4_moe_sort_aux": (_c_int, [_i32p, _c_int, _c_int, _c_int, _c_int, _i32p, _i32p, _i32p, _i32p, _i32p, _vp,
+                                   _c_size, _vp]),
     "a4w4_moe_gemm1_workspace_bytes": (_c_size, [_c_int, _c_int]),
     "a4w4_moe_gemm1": (_c_int, [_vp, _c_int, _c_int, _i32p, _i32p, _i32p, _c_int, _vp, _vp, _c_int, _c_int,
                                 _vp, _vp, _vp, _c_size, _vp]),
@@ -183,6 +186,17 @@ def a4w4_moe_sort(topk_ids, T, topk, E, block_m, sorted_rows, block_expert, num_
     _check("a4w4_moe_sort", lib().a4w4_moe_sort(_ptr(topk_ids), T, topk, E, block_m, _ptr(sorted_rows),
                                                 _ptr(block_expert), _ptr(num_blocks), _ptr(ws), ws_bytes,
                                                 _stream(stream)))
+
+
+def a4w4_moe_sort_aux_workspace_bytes(T, topk, E):
+    return lib().a4w4_moe_sort_aux_workspace_bytes(T, topk, E)
+
+
+def a4w4_moe_sort_aux(topk_ids, T, topk, E, block_m, sorted_rows, block_expert, num_blocks, sorted_tokens, row_slot,
+                      ws, ws_bytes, stream=None):
+    _check("a4w4_moe_sort_aux", lib().a4w4_moe_sort_aux(_ptr(topk_ids), T, topk, E, block_m, _ptr(sorted_rows),
+                                                        _ptr(block_expert), _ptr(num_blocks), _ptr(sorted_tokens),
+                                                        _ptr(row_slot), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def a4w4_moe_gemm1_workspace_bytes(T, D):

@@ -233,6 +233,31 @@ int a4w4_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, 
                                as_stream(stream));
 }
 
+size_t a4w4_moe_sort_aux_workspace_bytes(int T, int topk, int E) {
+  if (T <= 0 || topk <= 0 || E <= 0) return 0;
+  return a4w4::moe_sort_aux_ws_bytes(T, topk, E, sizing_sms());
+}
+
+int a4w4_moe_sort_aux(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
+                      int32_t* block_expert, int32_t* num_blocks, int32_t* sorted_tokens, int32_t* row_slot,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (T <= 0 || topk <= 0 || E <= 0 || E > 4096) return A4W4_ERR_ARG;
+  if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) return A4W4_ERR_ARG;
+  if (topk_ids == nullptr || sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr ||
+      sorted_tokens == nullptr || row_slot == nullptr)
+    return A4W4_ERR_ARG;
+  const int sms = current_device_sms();
+  if (sms < 0) return sms;
+  if (static_cast<long long>(T) * topk > static_cast<long long>(sms) * 32768) return A4W4_ERR_ARG;
+  if (!aligned16(ws) || ws_bytes < a4w4::moe_sort_aux_ws_bytes(T, topk, E, sms)) return A4W4_ERR_WORKSPACE;
+  unsigned int* status = status_ptr();
+  if (status == nullptr) return A4W4_ERR_LAUNCH;
+  const int rc = a4w4::launch_moe_sort_aux(topk_ids, T, topk, E, block_m, sorted_rows, block_expert, num_blocks,
+                                           sorted_tokens, row_slot, ws, as_stream(stream), sms,
+                                           g_wait_ns.load(std::memory_order_relaxed), status);
+  return rc == -1 ? A4W4_ERR_ARG : rc;
+}
+
 size_t a4w4_moe_gemm1_workspace_bytes(int T, int D) {
   if (T <= 0 || D <= 0) return 0;
   return static_cast<size_t>(T) * (D / 2) + static_cast<size_t>(T) * (D / 32);

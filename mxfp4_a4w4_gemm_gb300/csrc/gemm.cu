@@ -983,7 +983,7 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
   a.A = static_cast<const uint16_t*>(X);
   a.Wq = static_cast<const uint8_t*>(W1q);
   a.Ws = static_cast<const uint8_t*>(W1s);
-  const int rows = act == kActSilu ? I : 2 * I;     // weight rows per expert
+  const int rows = act == kActSwiglu ? 2 * I : I;     // weight rows per expert (SwiGLU: gate + up)
   a.M = T; a.N = rows; a.K = D; a.KT = (D + 255) / 256; a.splits = 1; a.w_tiles = rows / 256;
   a.wait_ns = wait_ns;
   a.sorted_rows = sorted_rows;

@@ -111,5 +111,11 @@ int launch_moe_sum(const float* partial, int T, int topk, int D, void* Y, cudaSt
 int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,
                     int32_t* block_expert, int32_t* num_blocks, void* ws, cudaStream_t st);
 size_t moe_sort_ws_bytes(int T, int topk, int E);
+// Single-launch sort with gather/scatter arrays (cooperative; E <= 4096,
+// T*topk <= sms * 32768).  Workspace: histograms + 2 barrier words, zeroed once.
+int launch_moe_sort_aux(const int32_t* ids, int T, int topk, int E, int bm, int32_t* sorted_rows,
+                        int32_t* block_expert, int32_t* num_blocks, int32_t* sorted_tokens, int32_t* row_slot,
+                        void* ws, cudaStream_t st, int sms, unsigned long long wait_ns, unsigned int* status);
+size_t moe_sort_aux_ws_bytes(int T, int topk, int E, int sms);
 
 }  // namespace a4w4

@@ -66,6 +66,24 @@ def sort_routed_rows(topk_ids, num_experts, block_m):
             len(experts))
 
 
+def sort_aux_arrays(sorted_rows, num_tokens, topk):
+    """Gather and scatter indices that accompany the sort ("[HIP] [CK]
+    [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4", Summary: the
+    adaptive MoE auxiliary sort; the review names the aux arrays that the sort
+    emits for A4W4).  Reading: for every sorted slot s, the token whose row
+    it holds (sorted_tokens[s] = sorted_rows[s] // topk, or num_tokens for a
+    padding slot), and for every routed row r the slot that holds it
+    (row_slot[sorted_rows[s]] = s).  Returns (sorted_tokens, row_slot), int32."""
+    rows = np.asarray(sorted_rows, dtype=np.int64)
+    sentinel = num_tokens * topk
+    tokens = np.where(rows < sentinel, rows // topk, num_tokens)
+    row_slot = np.full(sentinel, -1, dtype=np.int64)
+    for s, r in enumerate(rows):
+        if r < sentinel:
+            row_slot[r] = s
+    return tokens.astype(np.int32), row_slot.astype(np.int32)
+
+
 def silu(g):
     with np.errstate(over="ignore"):
         return g / (1.0 + np.exp(-g))

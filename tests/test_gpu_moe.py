@@ -58,6 +58,43 @@ def test_sort_bit_exact(T, bm):
     assert np.array_equal(bexp.cpu().numpy()[:enb], ee)
 
 
+def run_sort_aux(ids, n_exp, bm, ws=None):
+    T, topk = ids.shape
+    maxb = a4w4.a4w4_moe_max_blocks(T, topk, n_exp, bm)
+    rows = torch.full((maxb * bm,), -7, dtype=torch.int32, device="cuda")
+    toks = torch.full((maxb * bm,), -7, dtype=torch.int32, device="cuda")
+    slot = torch.full((T * topk,), -7, dtype=torch.int32, device="cuda")
+    bexp = torch.full((maxb,), -7, dtype=torch.int32, device="cuda")
+    nb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsb = a4w4.a4w4_moe_sort_aux_workspace_bytes(T, topk, n_exp)
+    if ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        a4w4.a4w4_workspace_init(ws, wsb)
+    a4w4.a4w4_moe_sort_aux(torch.from_numpy(ids).cuda(), T, topk, n_exp, bm, rows, bexp, nb, toks, slot, ws, wsb)
+    assert a4w4.a4w4_get_device_status() == 0
+    return rows, bexp, nb, toks, slot, ws
+
+
+@pytest.mark.parametrize("T,n_exp,topk", [(1, E, TOPK), (16, E, TOPK), (256, E, TOPK), (4096, E, TOPK),
+                                          (37, 5, 3), (3000, 64, 8), (1, 4096, 1)])
+@pytest.mark.parametrize("bm", [16, 128])
+def test_sort_aux_bit_exact(T, n_exp, topk, bm):
+    """The single-launch sort: sorted rows, block experts and block count equal
+    the oracle's, and the gather/scatter arrays equal the oracle's; twice in a
+    row on one workspace (the grid barrier resets itself)."""
+    ids = workloads.moe_topk_ids(T, n_exp, topk)
+    er, ee, enb = moe.sort_routed_rows(ids, n_exp, bm)
+    et, es = moe.sort_aux_arrays(er, T, topk)
+    ws = None
+    for _ in range(2):
+        rows, bexp, nb, toks, slot, ws = run_sort_aux(ids, n_exp, bm, ws)
+        assert int(nb.item()) == enb
+        assert np.array_equal(rows.cpu().numpy()[:enb * bm], er)
+        assert np.array_equal(bexp.cpu().numpy()[:enb], ee)
+        assert np.array_equal(toks.cpu().numpy()[:enb * bm], et)
+        assert np.array_equal(slot.cpu().numpy(), es)
+
+
 def h_error_bound(out):
     """Per-element bound on |h_gpu - h|: fp32 accumulation of 3584/64 = 56 MMA
     partial sums (at most 56 * 2^-24 < 2^-18 of sum|x w|), then silu and the

@@ -218,3 +218,24 @@ def test_gemm2_weights_scale_and_rows_sum_per_token():
     # a subset of tokens gives those rows of the full result
     ys, _, _ = moe.gemm2_tokens(q, s, ids, wts, f, [3, 1])
     assert np.array_equal(ys, y[[3, 1]])
+
+
+def test_sort_aux_arrays_by_hand_and_invariants():
+    ids = np.array([[2, 0], [0, 3], [2, 1]])
+    rows, experts, nb = moe.sort_routed_rows(ids, 4, 2)          # [1, 2, 5, S, 0, 4, 3, S]
+    tok, slot = moe.sort_aux_arrays(rows, 3, 2)
+    assert list(tok) == [0, 1, 2, 3, 0, 2, 1, 3]                 # token of each slot, T for padding
+    assert list(slot) == [4, 0, 1, 6, 5, 2]                      # slot of each routed row
+    for T in (1, 37, 256):
+        ids = workloads.moe_topk_ids(T, 896, 16)
+        for bm in (16, 128):
+            rows, experts, nb = moe.sort_routed_rows(ids, 896, bm)
+            tok, slot = moe.sort_aux_arrays(rows, T, 16)
+            assert np.array_equal(rows[slot], np.arange(T * 16))       # inverse permutation
+            real = rows < T * 16
+            assert np.array_equal(tok[real], rows[real] // 16) and np.all(tok[~real] == T)
+            # a block's tokens are distinct (topk experts per token are distinct)
+            for b in range(nb):
+                t = tok[b * bm:(b + 1) * bm]
+                t = t[t < T]
+                assert np.unique(t).size == t.size
