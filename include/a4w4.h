@@ -57,7 +57,9 @@ enum {
  *
  * Preshuffled layout (GB300 tensor-core operand tiles; KP = K rounded up to a
  * multiple of 256, KT = KP / 256, row tiles of 128 rows, nt = n / 128,
- * kt = k / 256, r = n % 128, atom = nt * KT + kt):
+ * kt = k / 256, r = n % 128, atom = ((nt / 2) * KT + kt) * 2 + nt % 2: the two
+ * 128-row atoms of a 256-row tile and one K tile are adjacent, so a GEMM tile
+ * fetches them with one bulk copy):
  *   Wq: atom-major tiles of 16384 bytes.  Byte b (0..127) of row r of a tile
  *       holds the codes of k = kt*256 + 2b (low nibble) and 2b+1 (high nibble)
  *       at offset  atom*16384 + (r/8)*1024 + (r%8)*128 + ((b/16) ^ (r%8))*16 + b%16

@@ -349,9 +349,10 @@ int a4w4_debug_gemm_export(const void* A_bf16, int M, int K, const void* Wq, con
   const int rc = gemm_impl(A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, ws_bytes, 0u, stream,
                            pl.prequant ? a4w4::ActDump{} : d);
   if (rc != A4W4_OK || !pl.prequant) return rc;
+  // the workspace holds 17 KB atoms (codes, then scales): split them
   const uint8_t* w8 = static_cast<const uint8_t*>(workspace);
-  if (cudaMemcpyAsync(d.codes, w8, atoms * 16384, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(d.scales, w8 + atoms * 16384, atoms * 1024, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+  if (cudaMemcpy2DAsync(d.codes, 16384, w8, 17408, 16384, atoms, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+      cudaMemcpy2DAsync(d.scales, 1024, w8 + 16384, 17408, 1024, atoms, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return A4W4_ERR_LAUNCH;
   return A4W4_OK;
 }

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(DCfg<NX, SW, SX>::THREADS, DCfg<NX, SW, SX>::M
   const uint64_t pol = policy_evict_first();   // every weight byte is read once
   auto issue_w = [&](int i) {
     const int s = i % SW;
-    const long long atom = static_cast<long long>(w_tile) * p.KT + (kt0 + i);
+    const long long atom = weight_atom(w_tile, kt0 + i, p.KT);
     mbar_arrive_expect_tx(full_w(s), Cf::W_STAGE + Cf::WSF_STAGE);
     bulk_g2s(base + Cf::OFF_W + s * Cf::W_STAGE, p.Wq + atom * 16384, 16384, full_w(s), pol);
     bulk_g2s(base + Cf::OFF_WSF + s * Cf::WSF_STAGE, p.Ws + atom * 1024, 1024, full_w(s), pol);

@@ -308,6 +308,14 @@ __device__ __forceinline__ uint32_t quant32_f32(const float* h, uint32_t* codes)
   return code;
 }
 
+// Weight operand layout (a4w4.h): 128-row x 256-K atoms grouped in pairs of
+// row tiles, so that a 256-row tile's two atoms of one K tile are adjacent:
+// atom (nt, kt) is number ((nt / 2) * KT + kt) * 2 + nt % 2, at 16 KB (codes)
+// and 1 KB (scales) per atom.
+__device__ __forceinline__ long long weight_atom(int nt, int kt, int KT) {
+  return (static_cast<long long>(nt >> 1) * KT + kt) * 2 + (nt & 1);
+}
+
 __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -83,6 +83,9 @@ struct Cfg {
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
   static constexpr bool kTmaA = MODE == kPre || MODE == kMoe2;   // activations arrive by TMA too
+  // kPre's activation tiles (written by the pre-pass) hold each atom's codes
+  // and scales in one 17 KB block: one bulk copy per stage
+  static constexpr bool kAInter = MODE == kPre;
   static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;  // MoE GEMM1
   static constexpr bool kRouted = kMoeAny || MODE == kMoe2;        // blocks of sorted routed rows
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
@@ -94,9 +97,9 @@ struct Cfg {
   static constexpr int THREADS = 32 * (2 + QWARPS);
   static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
   static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
-  static constexpr int X_CODE_BYTES = NX * 128;
+  static constexpr int X_CODE_BYTES = NX * 128 + (kAInter ? 1024 : 0);
   static constexpr int W_SF_BYTES = W_ATOMS * 1024;
-  static constexpr int X_SF_BYTES = 1024;
+  static constexpr int X_SF_BYTES = kAInter ? 0 : 1024;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_X = OFF_W + STAGES * W_CODE_BYTES;
   static constexpr int OFF_WSF = OFF_X + STAGES * X_CODE_BYTES;
@@ -209,15 +212,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     mbar_arrive_expect_tx(full_w(s), (Cf::W_ATOMS + (Cf::kTmaA ? 1 : 0)) * (16384 + 1024));
     if (Cf::kTmaA) {
       const long long atom = static_cast<long long>(x_tile) * p.KT + (kt0 + i);
-      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
-      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
+      if (Cf::kAInter) {
+        bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 17408, 17408, full_w(s), pol_a);
+      } else {
+        bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
+        bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
+      }
     }
-#pragma unroll
-    for (int a = 0; a < Cf::W_ATOMS; ++a) {
-      const long long atom = static_cast<long long>(w_tile * Cf::W_ATOMS + a) * p.KT + (kt0 + i);
-      bulk_g2s(base + Cf::OFF_W + s * Cf::W_CODE_BYTES + a * 16384, wq_e + atom * 16384, 16384, full_w(s), pol);
-      bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES + a * 1024, ws_e + atom * 1024, 1024, full_w(s), pol);
-    }
+    // the W_ATOMS atoms of this K tile are adjacent (weight_atom): one copy
+    // of codes, one of scales
+    const long long watom = weight_atom(w_tile * Cf::W_ATOMS, kt0 + i, p.KT);
+    bulk_g2s(base + Cf::OFF_W + s * Cf::W_CODE_BYTES, wq_e + watom * 16384, Cf::W_ATOMS * 16384, full_w(s), pol);
+    bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES, ws_e + watom * 1024, Cf::W_ATOMS * 1024, full_w(s), pol);
   };
   int issued = 0;
   if (warp == 0 && lane == 0) {
@@ -269,11 +275,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       bool ok = true;
       const uint32_t a_tile0 = base + (Cf::kSwapAB ? Cf::OFF_W : Cf::OFF_X);
       const uint32_t b_tile0 = base + (Cf::kSwapAB ? Cf::OFF_X : Cf::OFF_W);
-      const uint32_t a_sf0 = base + (Cf::kSwapAB ? Cf::OFF_WSF : Cf::OFF_XSF);
+      const uint32_t a_sf0 = base + (Cf::kSwapAB ? Cf::OFF_WSF : (Cf::kAInter ? Cf::OFF_X + 16384 : Cf::OFF_XSF));
       const uint32_t b_sf0 = base + (Cf::kSwapAB ? Cf::OFF_XSF : Cf::OFF_WSF);
       constexpr uint32_t A_STAGE = Cf::kSwapAB ? Cf::W_CODE_BYTES : Cf::X_CODE_BYTES;
       constexpr uint32_t B_STAGE = Cf::kSwapAB ? Cf::X_CODE_BYTES : Cf::W_CODE_BYTES;
-      constexpr uint32_t ASF_STAGE = Cf::kSwapAB ? Cf::W_SF_BYTES : Cf::X_SF_BYTES;
+      constexpr uint32_t ASF_STAGE = Cf::kSwapAB ? Cf::W_SF_BYTES : (Cf::kAInter ? Cf::X_CODE_BYTES : Cf::X_SF_BYTES);
       constexpr uint32_t BSF_STAGE = Cf::kSwapAB ? Cf::X_SF_BYTES : Cf::W_SF_BYTES;
       const uint64_t adesc0 = sdesc_sw128(a_tile0), bdesc0 = sdesc_sw128(b_tile0);
       const uint64_t asfd0 = sdesc_sf(a_sf0), bsfd0 = sdesc_sf(b_sf0);
@@ -942,8 +948,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   a.C = static_cast<uint16_t*>(C);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   if (pl.prequant) {
-    a.Aq = w8;
-    a.As = w8 + static_cast<size_t>(pl.x_tiles) * pl.kt * 16384;
+    a.Aq = w8;               // 17 KB atoms: codes then scales
     w8 += pl.aq_bytes;
   }
   if (pl.splits > 1 && !pl.cluster_reduce) {
@@ -965,7 +970,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   if (pl.prequant) {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int rc = launch_quant_activation_tiles(A, M, K, const_cast<uint8_t*>(a.Aq), const_cast<uint8_t*>(a.As), st, sms);
+    const int rc = launch_quant_activation_tiles(A, M, K, const_cast<uint8_t*>(a.Aq), st, sms);
     if (rc != 0) return rc;
     return launch_cfg<kPre, 128, 4>(a, grid, st);
   }

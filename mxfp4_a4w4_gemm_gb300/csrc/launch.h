@@ -83,8 +83,10 @@ struct ActDump {
 int launch_mxfp4_quant(const void* x, long long rows, int cols, void* q, void* s, cudaStream_t st, int sms);
 int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_I, void* wq, void* ws,
                           cudaStream_t st, int sms);
-// A [M, K] -> MXFP4 in the weight tile layout (rows padded to 128 with zeros).
-int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms);
+// A [M, K] -> MXFP4 tiles of 128 rows x 256 K (rows padded to 128 with zeros),
+// atom x*KT + kt at aq + atom*17408: 16 KB of codes in the weight tile layout,
+// then its 1 KB of scales.
+int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, cudaStream_t st, int sms);
 // prefetch_w: weights may be read before the previous grid on the stream
 // completes (the caller guarantees that grid does not write them).
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,

@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kAuxThreads, 1)
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(aux_sh);
   int32_t* start = aux_sh + (kAuxWarps * E + 1) / 2;   // [E] first slot of the expert's rows from this CTA
   int32_t* total = start + E;                          // [E] rows routed to the expert
-  int32_t* scan_tmp = total + E;                       // [kAuxThreads]
+  int32_t* first_blk = total + E;                      // [E] the expert's first block
+  int32_t* scan_tmp = first_blk + E;                   // [kAuxThreads]
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
@@ -259,19 +260,22 @@ __global__ void __launch_bounds__(kAuxThreads, 1)
   int boff = scan_tmp[threadIdx.x] - nb_local;    // first block of expert e0
   if (c == 0 && threadIdx.x == kAuxThreads - 1) *num_blocks = scan_tmp[threadIdx.x];
   for (int e = e0; e < e1; ++e) {
-    const int tot = total[e];
-    const int nb_e = (tot + bm - 1) / bm;
+    first_blk[e] = boff;
     start[e] += boff * bm;
-    if (e % G == c) {                              // this CTA writes expert e's block list and padding
-      for (int b = 0; b < nb_e; ++b) block_expert[boff + b] = e;
-      for (int sl = boff * bm + tot; sl < (boff + nb_e) * bm; ++sl) {
-        sorted_rows[sl] = n;                       // sentinel T * topk
-        sorted_tokens[sl] = T;
-      }
-    }
-    boff += nb_e;
+    boff += (total[e] + bm - 1) / bm;
   }
   __syncthreads();
+  // experts e = c (mod G): block list and padding sentinels, each expert's
+  // range written by a warp of this CTA (lanes over consecutive slots)
+  for (int e = c + warp * G; e < E; e += kAuxWarps * G) {
+    const int b0 = first_blk[e], tot = total[e];
+    const int nb_e = (tot + bm - 1) / bm;
+    for (int b = lane; b < nb_e; b += 32) block_expert[b0 + b] = e;
+    for (int sl = b0 * bm + tot + lane; sl < (b0 + nb_e) * bm; sl += 32) {
+      sorted_rows[sl] = n;                         // sentinel T * topk
+      sorted_tokens[sl] = T;
+    }
+  }
   // 4. place, stable: increasing r within each expert
   for (int s = r0; s < r1; s += 32) {
     const int r = s + lane;
@@ -318,10 +322,10 @@ int launch_moe_sort_aux(const int32_t* ids, int T, int topk, int E, int bm, int3
   if (per > kAuxMaxPerCta) return -1;
   const size_t hist_bytes = static_cast<size_t>(g) * E * sizeof(int32_t);
   unsigned int* bar = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + hist_bytes);
-  const size_t shm = static_cast<size_t>((kAuxWarps * E + 1) / 2 + 2 * E + kAuxThreads) * sizeof(int32_t);
+  const size_t shm = static_cast<size_t>((kAuxWarps * E + 1) / 2 + 3 * E + kAuxThreads) * sizeof(int32_t);
   static std::atomic<unsigned long long> attr_devs{0};
   if (ensure_func_attrs(attr_devs, [&] {
-        const int max_shm = ((kAuxWarps * kAuxMaxExperts + 1) / 2 + 2 * kAuxMaxExperts + kAuxThreads) * 4;
+        const int max_shm = ((kAuxWarps * kAuxMaxExperts + 1) / 2 + 3 * kAuxMaxExperts + kAuxThreads) * 4;
         return cudaFuncSetAttribute(moe_sort_aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_shm) ==
                cudaSuccess;
       }) != 0)

@@ -37,18 +37,22 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const uint4* __restric
 // One thread per (row, 32-block) of the padded matrix [rows, KP]; writes the
 // 16 code bytes into the 128-byte-swizzled tile and the scale byte into the
 // 128x4 scale atom (layout documented in a4w4.h).  Rows >= valid_rows (the
-// padding of an activation matrix to whole 128-row tiles) get zeros.  With
+// padding of an activation matrix to whole 128-row tiles) get zeros.
+// Weights (act_tiles == 0): atoms grouped in pairs of row tiles (weight_atom),
+// codes in wq, scales in ws.  Activation tiles of the quantise-once GEMM
+// (act_tiles == 1): atom nt*KT + kt holds its 16 KB of codes followed by its
+// 1 KB of scales at wq + atom * 17408, so one bulk copy brings both.  With
 // `pair_I` > 0 the preshuffled row n of each expert is gate row
 // 128*(n/256) + n%256 when n%256 < 128, else up row pair_I + 128*(n/256) + n%256 - 128.
 __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __restrict__ w, int rows, int valid_rows,
                                                              int K, int KT, int experts, int pair_I,
                                                              uint8_t* __restrict__ wq, uint8_t* __restrict__ ws,
-                                                             int early_trigger) {
+                                                             int act_tiles) {
   griddep_wait();                // w may come from the previous kernel on the stream
   // Activation tiles: the GEMM that follows waits for this grid before
   // reading them, so it may start its set-up now.  Weights: the trigger stays
   // at completion, since a GEMM with weight prefetch reads its weights early.
-  if (early_trigger) griddep_launch_dependents();
+  if (act_tiles) griddep_launch_dependents();
   const int kblocks = KT * 8;
   const long long total = static_cast<long long>(experts) * rows * kblocks;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -75,10 +79,17 @@ __global__ void __launch_bounds__(256) prepare_weight_kernel(const uint16_t* __r
       code = quant32_bf16(v, c);
     }
     const int nt = n / 128, r = n % 128, kt = kb / 8, j = kb % 8;
-    const long long atom = static_cast<long long>(e) * (rows / 128) * KT + static_cast<long long>(nt) * KT + kt;
-    uint8_t* dst = wq + atom * 16384 + (r / 8) * 1024 + (r % 8) * 128 + ((j ^ (r % 8)) * 16);
-    *reinterpret_cast<uint4*>(dst) = make_uint4(c[0], c[1], c[2], c[3]);
-    ws[atom * 1024 + (j / 4) * 512 + (r % 32) * 16 + (r / 32) * 4 + (j % 4)] = static_cast<uint8_t>(code);
+    const uint32_t code_off = (r / 8) * 1024 + (r % 8) * 128 + ((j ^ (r % 8)) * 16);
+    const uint32_t sf_off = (j / 4) * 512 + (r % 32) * 16 + (r / 32) * 4 + (j % 4);
+    if (act_tiles) {
+      uint8_t* at = wq + (static_cast<long long>(nt) * KT + kt) * 17408;
+      *reinterpret_cast<uint4*>(at + code_off) = make_uint4(c[0], c[1], c[2], c[3]);
+      at[16384 + sf_off] = static_cast<uint8_t>(code);
+    } else {
+      const long long atom = static_cast<long long>(e) * (rows / 128) * KT + weight_atom(nt, kt, KT);
+      *reinterpret_cast<uint4*>(wq + atom * 16384 + code_off) = make_uint4(c[0], c[1], c[2], c[3]);
+      ws[atom * 1024 + sf_off] = static_cast<uint8_t>(code);
+    }
   }
 }
 
@@ -104,12 +115,12 @@ int launch_prepare_weight(const void* w, int rows, int K, int experts, int pair_
                     rows, rows, K, KT, experts, pair_I, static_cast<uint8_t*>(wq), static_cast<uint8_t*>(ws), 0);
 }
 
-int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, void* as, cudaStream_t st, int sms) {
+int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, cudaStream_t st, int sms) {
   const int KT = (K + 255) / 256;
   const int rows = (M + 127) / 128 * 128;
   const long long items = static_cast<long long>(rows) * KT * 8;
   return launch_pdl(prepare_weight_kernel, grid_for(items, 256, sms, 8), 256, st, static_cast<const uint16_t*>(a),
-                    rows, M, K, KT, 1, 0, static_cast<uint8_t*>(aq), static_cast<uint8_t*>(as), 1);
+                    rows, M, K, KT, 1, 0, static_cast<uint8_t*>(aq), static_cast<uint8_t*>(nullptr), 1);
 }
 
 }  // namespace a4w4

@@ -66,9 +66,16 @@ def shuffle_tiles(codes, scales, rows, tiles, KT):
 
 def unshuffle_weight(wq, ws, N, K):
     """Preshuffled weights (include/a4w4.h) -> plain packed codes [N, KP/2] and
-    E8M0 scales [N, KP/32] (KP = K rounded up to 256)."""
+    E8M0 scales [N, KP/32] (KP = K rounded up to 256).  Atom (nt, kt) is
+    number ((nt // 2) * KT + kt) * 2 + nt % 2; the atoms are put back in
+    (nt, kt) order, then read with unshuffle_tiles."""
     KT = -(-K // 256)
-    return unshuffle_tiles(wq, ws, 128, N // 128, KT)
+    nt = np.arange(N // 128)[:, None]
+    kt = np.arange(KT)[None, :]
+    order = (((nt // 2) * KT + kt) * 2 + nt % 2).reshape(-1)       # atom number of (nt, kt), row-major
+    wq = np.asarray(wq, dtype=np.uint8).reshape(-1, 16384)[order]
+    ws = np.asarray(ws, dtype=np.uint8).reshape(-1, 1024)[order]
+    return unshuffle_tiles(wq.reshape(-1), ws.reshape(-1), 128, N // 128, KT)
 
 
 def gemm_violations(c_bits, ref, abs_sum):
