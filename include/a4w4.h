@@ -161,18 +161,20 @@ int a4w4_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m,
                   int32_t* sorted_rows, int32_t* block_expert, int32_t* num_blocks,
                   void* ws, size_t ws_bytes, void* stream);
 
-/* The same sort in one launch, with the auxiliary gather/scatter arrays.
+/* The same sort, with the auxiliary gather/scatter arrays, in one launch for
+ * up to 2048 routed rows and two beyond.
  * "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4",
  * Summary (the adaptive MoE auxiliary sort; its review names the aux arrays
  * the sort emits for A4W4).  sorted_rows, block_expert and num_blocks are
  * identical to a4w4_moe_sort's; in addition sorted_tokens[s] is the token
  * (r / topk) of sorted slot s, or T for a padding slot (same length as
  * sorted_rows), and row_slot[r] is the slot that holds routed row r (int32
- * [T*topk]).  One cooperative launch of up to one CTA per SM, one CTA for up
- * to 2048 routed rows (a decode batch).  E <= 4096, T*topk <= 32768 x the
- * SM count.  ws >= a4w4_moe_sort_aux_workspace_bytes(T, topk, E) bytes, 16-byte
- * aligned, zeroed once with a4w4_workspace_init (it ends with a grid barrier
- * that resets itself; re-initialise after a TIMEOUT). */
+ * [T*topk]).  Up to 2048 routed rows (a decode batch) one CTA does the whole
+ * sort; beyond, up to one CTA per SM each counts a run of rows, the last to
+ * finish scans the counts, and a second launch places the rows.  E <= 4096,
+ * T*topk <= 32768 x the SM count.  ws >= a4w4_moe_sort_aux_workspace_bytes(T,
+ * topk, E) bytes, 16-byte aligned, zeroed once with a4w4_workspace_init (it
+ * ends with a ticket counter that the last counting CTA resets). */
 size_t a4w4_moe_sort_aux_workspace_bytes(int T, int topk, int E);
 int a4w4_moe_sort_aux(const int32_t* topk_ids, int T, int topk, int E, int block_m,
                       int32_t* sorted_rows, int32_t* block_expert, int32_t* num_blocks,

@@ -136,64 +136,60 @@ int launch_moe_sort(const int32_t* ids, int T, int topk, int E, int bm, int32_t*
 }
 
 // ---------------------------------------------------------------------------
-// Single-launch sort with the auxiliary gather/scatter arrays ("[HIP] [CK]
-// [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4", Summary: the
-// adaptive MoE auxiliary sort).  Same sorted output as the three-launch sort
-// above, plus sorted_tokens[slot] (the token of each slot, T for padding) and
-// row_slot[r] (the slot of each routed row).  One cooperative launch of G CTAs
-// (1 for up to 2048 routed rows; at most one per SM), 16 warps each:
-//   1. each warp walks its contiguous run of entries 32 at a time;
-//      __match_any_sync groups equal experts and the leader adds the group to
-//      the warp's own per-expert count (shared memory, no atomics); the CTA
-//      publishes its per-expert totals;
-//   2. grid barrier (G > 1): an arrival counter and a generation word in the
-//      workspace, bounded spin;
-//   3. every CTA reads all G histograms: per expert its total, the rows of
-//      CTAs before it, the padded block count, and an exclusive scan over
-//      experts gives each expert's first slot; experts e = c (mod G) get their
-//      block_expert entries and padding sentinels from CTA c;
-//   4. each warp re-walks its run: slot = expert start + rows of earlier CTAs
-//      + rows of earlier warps + rows earlier in this warp + rank among equal
-//      lanes of the step (stable, increasing r within each expert).
+// Sort with the auxiliary gather/scatter arrays ("[HIP] [CK] [FlyDSL] [Kernel]
+// Extend MXFP4 GEMM1 replacement to A4W4", Summary: the adaptive MoE auxiliary
+// sort).  Same sorted output as the three-launch sort above, plus
+// sorted_tokens[slot] (the token of each slot, T for padding) and row_slot[r]
+// (the slot of each routed row).  Entries are split into G runs of per_cta
+// (one run per CTA, 16 warps, each warp a contiguous sub-run):
+//   count  each warp walks its sub-run 32 entries at a time; __match_any_sync
+//          groups equal experts and the group's leader adds it to the warp's
+//          per-expert count (shared memory, no atomics);
+//   scan   per expert: total, padded block count, an exclusive scan over
+//          experts gives each expert's first block; block_expert[], the block
+//          count and the padding sentinels are written (a warp per expert);
+//   place  each warp re-walks its sub-run: slot = expert's first slot + rows
+//          of earlier runs + rows of earlier warps + rows earlier in the warp
+//          + rank among equal lanes of the step (stable: increasing r).
+// Adaptive: up to 2048 routed rows (decode batches) one CTA does all three in
+// one launch; beyond, a counting launch whose last CTA to finish (atomic
+// ticket, no waiting) runs the scan, then a placing launch (programmatic
+// dependent launch: it counts its run again while the first one finishes).
 constexpr int kAuxWarps = 16;
 constexpr int kAuxThreads = kAuxWarps * 32;
 constexpr int kAuxMaxExperts = 4096;
 constexpr int kAuxMaxPerCta = 32768;   // keeps every per-warp offset below 2^16
+constexpr int kAuxRun = 2048;          // routed rows per CTA (at most one CTA per SM beyond)
 
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+struct AuxSmem {
+  uint16_t* wcnt;     // [kAuxWarps][E]: counts, then exclusive prefix over warps, then running cursors
+  int32_t* start;     // [E]
+  int32_t* total;     // [E]
+  int32_t* first;     // [E]
+  int32_t* scan;      // [kAuxThreads]
+};
+
+__device__ __forceinline__ AuxSmem aux_smem(int32_t* sh, int E) {
+  AuxSmem a;
+  a.wcnt = reinterpret_cast<uint16_t*>(sh);
+  a.start = sh + (kAuxWarps * E + 1) / 2;
+  a.total = a.start + E;
+  a.first = a.total + E;
+  a.scan = a.first + E;
+  return a;
 }
 
-__global__ void __launch_bounds__(kAuxThreads, 1)
-    moe_sort_aux_kernel(const int32_t* __restrict__ ids, int n, int topk, int T, int E, int bm, int per_cta,
-                        int32_t* __restrict__ sorted_rows, int32_t* __restrict__ block_expert,
-                        int32_t* __restrict__ num_blocks, int32_t* __restrict__ sorted_tokens,
-                        int32_t* __restrict__ row_slot, int32_t* __restrict__ hist, unsigned int* bar,
-                        unsigned long long wait_ns, unsigned int* status) {
-  extern __shared__ int32_t aux_sh[];
-  // [kAuxWarps][E] per-warp counts, then each warp's running offset within
-  // the CTA (both <= per_cta <= kAuxMaxPerCta, so 16 bits suffice)
-  uint16_t* wcnt = reinterpret_cast<uint16_t*>(aux_sh);
-  int32_t* start = aux_sh + (kAuxWarps * E + 1) / 2;   // [E] first slot of the expert's rows from this CTA
-  int32_t* total = start + E;                          // [E] rows routed to the expert
-  int32_t* first_blk = total + E;                      // [E] the expert's first block
-  int32_t* scan_tmp = first_blk + E;                   // [kAuxThreads]
-  __shared__ int abort_flag;
+// Per-warp counts of this CTA's run -> exclusive prefix over the warps
+// (wcnt), and the run's per-expert totals into hist_row (global) when given,
+// else into a.total.
+__device__ void aux_count(const int32_t* __restrict__ ids, int r0, int r1, int E, AuxSmem a, int32_t* hist_row) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x, c = blockIdx.x;
-  for (int i = threadIdx.x; i < kAuxWarps * E; i += kAuxThreads) wcnt[i] = 0;
-  if (threadIdx.x == 0) abort_flag = 0;
+  for (int i = threadIdx.x; i < kAuxWarps * E; i += kAuxThreads) a.wcnt[i] = 0;
   __syncthreads();
-  const int per_warp = per_cta / kAuxWarps;
-  const int r0 = c * per_cta + warp * per_warp;
-  const int r1 = min(n, r0 + per_warp);
-  uint16_t* my = wcnt + warp * E;
-  // 1. per-warp counts; the CTA's totals to global memory
+  uint16_t* my = a.wcnt + warp * E;
   for (int s = r0; s < r1; s += 32) {
     const int r = s + lane;
-    int e = r < r1 ? ids[r] : -1;
+    int e = r < r1 ? __ldcg(ids + r) : -1;   // L2: ids may be read before a dependency wait
     const bool ok = e >= 0 && e < E;
     if (!ok) e = -1 - lane;                       // unique key: matches no other lane
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
@@ -202,96 +198,86 @@ __global__ void __launch_bounds__(kAuxThreads, 1)
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kAuxThreads) {
     int tot = 0;
-    for (int w = 0; w < kAuxWarps; ++w) {         // counts -> exclusive prefix over the warps
-      const int v = wcnt[w * E + e];
-      wcnt[w * E + e] = static_cast<uint16_t>(tot);
+    for (int w = 0; w < kAuxWarps; ++w) {
+      const int v = a.wcnt[w * E + e];
+      a.wcnt[w * E + e] = static_cast<uint16_t>(tot);
       tot += v;
     }
-    hist[static_cast<long long>(c) * E + e] = tot;
+    if (hist_row != nullptr) hist_row[e] = tot;
+    else a.total[e] = tot;
   }
-  // 2. grid barrier (one CTA: a block barrier suffices)
   __syncthreads();
-  if (G > 1) {
-    if (threadIdx.x == 0) {
-      const unsigned int gen = ld_acquire_u32(bar + 1);
-      __threadfence();
-      if (atomicAdd(bar, 1u) == static_cast<unsigned int>(G - 1)) {
-        bar[0] = 0u;
-        __threadfence();
-        atomicAdd(bar + 1, 1u);                   // release the others
-      } else {
-        const uint64_t t0 = global_timer_ns();
-        while (ld_acquire_u32(bar + 1) == gen) {
-          if (global_timer_ns() - t0 > wait_ns) {
-            atomicOr(status, kStatusTimeout);
-            abort_flag = 1;
-            break;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    if (abort_flag) return;
-  }
-  // 3. per expert: total, rows of earlier CTAs, padded blocks; exclusive scan
-  //    of the block counts over experts (thread order = expert order)
+}
+
+// Scan over experts of the totals in a.total: first block per expert into
+// a.first (and `first_out` when not null); block_expert[], *num_blocks and
+// the padding sentinels.
+__device__ void aux_scan(int E, int bm_log2, int n, int T, AuxSmem a, int32_t* __restrict__ sorted_rows,
+                         int32_t* __restrict__ block_expert, int32_t* __restrict__ num_blocks,
+                         int32_t* __restrict__ sorted_tokens, int32_t* first_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bm = 1 << bm_log2;
   const int per_t = (E + kAuxThreads - 1) / kAuxThreads;
   const int e0 = min(E, threadIdx.x * per_t), e1 = min(E, e0 + per_t);
   int nb_local = 0;
-  for (int e = e0; e < e1; ++e) {
-    int tot = 0, before = 0;
-    for (int g = 0; g < G; ++g) {
-      const int v = __ldcg(hist + static_cast<long long>(g) * E + e);
-      if (g < c) before += v;
-      tot += v;
-    }
-    start[e] = before;
-    total[e] = tot;
-    nb_local += (tot + bm - 1) / bm;
-  }
-  scan_tmp[threadIdx.x] = nb_local;
+  for (int e = e0; e < e1; ++e) nb_local += (a.total[e] + bm - 1) >> bm_log2;
+  a.scan[threadIdx.x] = nb_local;
   __syncthreads();
   for (int d = 1; d < kAuxThreads; d <<= 1) {
-    const int v = threadIdx.x >= d ? scan_tmp[threadIdx.x - d] : 0;
+    const int v = threadIdx.x >= d ? a.scan[threadIdx.x - d] : 0;
     __syncthreads();
-    scan_tmp[threadIdx.x] += v;
+    a.scan[threadIdx.x] += v;
     __syncthreads();
   }
-  int boff = scan_tmp[threadIdx.x] - nb_local;    // first block of expert e0
-  if (c == 0 && threadIdx.x == kAuxThreads - 1) *num_blocks = scan_tmp[threadIdx.x];
+  int boff = a.scan[threadIdx.x] - nb_local;
+  if (threadIdx.x == kAuxThreads - 1) *num_blocks = a.scan[threadIdx.x];
   for (int e = e0; e < e1; ++e) {
-    first_blk[e] = boff;
-    start[e] += boff * bm;
-    boff += (total[e] + bm - 1) / bm;
+    a.first[e] = boff;
+    if (first_out != nullptr) first_out[e] = boff;
+    boff += (a.total[e] + bm - 1) >> bm_log2;
   }
   __syncthreads();
-  // experts e = c (mod G): block list and padding sentinels, each expert's
-  // range written by a warp of this CTA (lanes over consecutive slots)
-  for (int e = c + warp * G; e < E; e += kAuxWarps * G) {
-    const int b0 = first_blk[e], tot = total[e];
-    const int nb_e = (tot + bm - 1) / bm;
-    for (int b = lane; b < nb_e; b += 32) block_expert[b0 + b] = e;
-    for (int sl = b0 * bm + tot + lane; sl < (b0 + nb_e) * bm; sl += 32) {
-      sorted_rows[sl] = n;                         // sentinel T * topk
-      sorted_tokens[sl] = T;
+  // block lists and padding of the experts that have rows: each warp scans 32
+  // experts at a time and handles the non-empty ones together (lanes over slots)
+  for (int base = warp * 32; base < E; base += kAuxWarps * 32) {
+    const int me = base + lane;
+    unsigned hit = __ballot_sync(0xFFFFFFFFu, me < E && a.total[me] > 0);
+    while (hit) {
+      const int e = base + __ffs(hit) - 1;
+      hit &= hit - 1;
+      const int b0 = a.first[e], tot = a.total[e];
+      const int nb_e = (tot + bm - 1) >> bm_log2;
+      for (int b = lane; b < nb_e; b += 32) block_expert[b0 + b] = e;
+      for (int sl = (b0 << bm_log2) + tot + lane; sl < ((b0 + nb_e) << bm_log2); sl += 32) {
+        sorted_rows[sl] = n;                        // sentinel T * topk
+        sorted_tokens[sl] = T;
+      }
     }
   }
-  // 4. place, stable: increasing r within each expert
+}
+
+// Stable placement of this CTA's run (a.start holds each expert's first slot
+// for this run; a.wcnt each warp's prefix).
+__device__ void aux_place(const int32_t* __restrict__ ids, int r0, int r1, int E, int topk, AuxSmem a,
+                          int32_t* __restrict__ sorted_rows, int32_t* __restrict__ sorted_tokens,
+                          int32_t* __restrict__ row_slot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint16_t* my = a.wcnt + warp * E;
   for (int s = r0; s < r1; s += 32) {
     const int r = s + lane;
-    int e = r < r1 ? ids[r] : -1;
+    int e = r < r1 ? __ldcg(ids + r) : -1;
     const bool ok = e >= 0 && e < E;
     if (!ok) e = -1 - lane;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int before = ok ? my[e] : 0;
     if (ok) {
-      const int slot = start[e] + before + rank;
+      const int slot = a.start[e] + before + rank;
       sorted_rows[slot] = r;
       sorted_tokens[slot] = r / topk;
       row_slot[r] = slot;
     } else if (r < r1) {
-      row_slot[r] = -1;                            // expert id outside [0, E): not routed
+      row_slot[r] = -1;                              // expert id outside [0, E): not routed
     }
     __syncwarp();
     if (ok && rank == 0) my[e] = static_cast<uint16_t>(before + __popc(peers));
@@ -299,51 +285,226 @@ __global__ void __launch_bounds__(kAuxThreads, 1)
   }
 }
 
-// CTAs of the aux sort: one per 2048 routed rows, at most one per SM.
+// One warp, up to 32 routed rows (a decode batch of one or two tokens): only
+// the experts that were hit are touched.  Lane i holds routed row i; a
+// bitonic sort of the keys expert*64 + row over the warp orders the rows by
+// expert, then by row; the first lane of each expert's run counts it, a scan
+// over those lanes gives each expert's first block.
+__global__ void __launch_bounds__(32, 1)
+    moe_sort_aux_warp(const int32_t* __restrict__ ids, int n, int topk, int T, int E, int bm,
+                      int32_t* __restrict__ sorted_rows, int32_t* __restrict__ block_expert,
+                      int32_t* __restrict__ num_blocks, int32_t* __restrict__ sorted_tokens,
+                      int32_t* __restrict__ row_slot) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x;
+  int e = lane < n ? __ldcg(ids + lane) : -1;
+  const bool ok = e >= 0 && e < E;
+  if (lane < n && !ok) row_slot[lane] = -1;        // expert id outside [0, E): not routed
+  // key: valid rows by (expert, row); everything else sorts last
+  unsigned key = ok ? (static_cast<unsigned>(e) << 6) | static_cast<unsigned>(lane) : 0xFFFFFFFFu;
+  for (int k = 2; k <= 32; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned other = __shfl_xor_sync(0xFFFFFFFFu, key, j);
+      const bool up = (lane & k) == 0;
+      const bool lower = (lane & j) == 0;
+      key = (lower == up) ? min(key, other) : max(key, other);
+    }
+  }
+  const bool valid = key != 0xFFFFFFFFu;
+  const int ke = valid ? static_cast<int>(key >> 6) : -1;
+  const int kr = static_cast<int>(key & 63u);
+  const int prev = __shfl_up_sync(0xFFFFFFFFu, ke, 1);
+  const bool head = valid && (lane == 0 || prev != ke);
+  const unsigned heads = __ballot_sync(0xFFFFFFFFu, head);
+  // run of this lane's expert: [start lane, next head)
+  const int run0 = 31 - __clz(heads & ((2u << lane) - 1u));        // last head at or before this lane
+  const unsigned later = heads & ~((2u << lane) - 1u);
+  const int nvalid = __popc(__ballot_sync(0xFFFFFFFFu, valid));
+  const int run1 = later ? __ffs(later) - 1 : nvalid;
+  const int cnt = run1 - run0;
+  const int nblk = head ? (cnt + bm - 1) / bm : 0;
+  int incl = nblk;                                  // inclusive scan of block counts over lanes
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  const int first = __shfl_sync(0xFFFFFFFFu, incl - nblk, run0);   // the run's first block
+  if (lane == 31) *num_blocks = incl;
+  if (valid) {
+    const int slot = first * bm + (lane - run0);
+    sorted_rows[slot] = kr;
+    sorted_tokens[slot] = kr / topk;
+    row_slot[kr] = slot;
+  }
+  // block lists and padding, a run at a time, lanes over slots
+  unsigned h = heads;
+  while (h) {
+    const int src = __ffs(h) - 1;
+    h &= h - 1;
+    const int re = __shfl_sync(0xFFFFFFFFu, ke, src);
+    const int rf = __shfl_sync(0xFFFFFFFFu, first, src);
+    const int rc = __shfl_sync(0xFFFFFFFFu, cnt, src);
+    const int rb = (rc + bm - 1) / bm;
+    for (int b = lane; b < rb; b += 32) block_expert[rf + b] = re;
+    for (int sl = rf * bm + rc + lane; sl < (rf + rb) * bm; sl += 32) {
+      sorted_rows[sl] = n;
+      sorted_tokens[sl] = T;
+    }
+  }
+}
+
+// One CTA, all three steps (n <= kAuxRun).
+__global__ void __launch_bounds__(kAuxThreads, 1)
+    moe_sort_aux_single(const int32_t* __restrict__ ids, int n, int topk, int T, int E, int bm,
+                        int32_t* __restrict__ sorted_rows, int32_t* __restrict__ block_expert,
+                        int32_t* __restrict__ num_blocks, int32_t* __restrict__ sorted_tokens,
+                        int32_t* __restrict__ row_slot) {
+  extern __shared__ int32_t aux_sh[];
+  griddep_wait();                                    // ids may come from the previous kernel
+  griddep_launch_dependents();
+  const AuxSmem a = aux_smem(aux_sh, E);
+  const int per_warp = (n + kAuxWarps * 32 - 1) / (kAuxWarps * 32) * 32;
+  const int warp = threadIdx.x >> 5;
+  const int r0 = min(n, warp * per_warp), r1 = min(n, r0 + per_warp);
+  aux_count(ids, r0, r1, E, a, nullptr);
+  aux_scan(E, 31 - __clz(bm), n, T, a, sorted_rows, block_expert, num_blocks, sorted_tokens, nullptr);
+  for (int e = threadIdx.x; e < E; e += kAuxThreads) a.start[e] = a.first[e] * bm;
+  __syncthreads();
+  aux_place(ids, r0, r1, E, topk, a, sorted_rows, sorted_tokens, row_slot);
+}
+
+// Counting launch (G CTAs): each CTA's run totals to hist[c][*]; the last CTA
+// to finish (atomic ticket in the workspace, reset by that CTA) runs the scan.
+__global__ void __launch_bounds__(kAuxThreads, 1)
+    moe_sort_aux_count(const int32_t* __restrict__ ids, int n, int T, int E, int bm, int per_cta,
+                       int32_t* __restrict__ sorted_rows, int32_t* __restrict__ block_expert,
+                       int32_t* __restrict__ num_blocks, int32_t* __restrict__ sorted_tokens,
+                       int32_t* __restrict__ hist, int32_t* __restrict__ first_out, unsigned int* ticket) {
+  extern __shared__ int32_t aux_sh[];
+  __shared__ int last;
+  griddep_wait();
+  griddep_launch_dependents();                       // the placing launch may start counting now
+  const AuxSmem a = aux_smem(aux_sh, E);
+  const int G = gridDim.x, c = blockIdx.x, warp = threadIdx.x >> 5;
+  const int per_warp = per_cta / kAuxWarps;
+  const int r0 = min(n, c * per_cta + warp * per_warp), r1 = min(n, r0 + per_warp);
+  aux_count(ids, r0, r1, E, a, hist + static_cast<long long>(c) * E);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(ticket, 1u) == static_cast<unsigned int>(G - 1);
+    if (last) *ticket = 0u;                          // ready for the next call
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < E; e += kAuxThreads) {
+    int tot = 0;
+    for (int g = 0; g < G; ++g) tot += __ldcg(hist + static_cast<long long>(g) * E + e);
+    a.total[e] = tot;
+  }
+  __syncthreads();
+  aux_scan(E, 31 - __clz(bm), n, T, a, sorted_rows, block_expert, num_blocks, sorted_tokens, first_out);
+}
+
+// Placing launch: counts its run again (the ids only) before waiting for the
+// counting launch, then reads the histograms and the experts' first blocks.
+__global__ void __launch_bounds__(kAuxThreads, 1)
+    moe_sort_aux_place(const int32_t* __restrict__ ids, int n, int topk, int E, int bm, int per_cta,
+                       int32_t* __restrict__ sorted_rows, int32_t* __restrict__ sorted_tokens,
+                       int32_t* __restrict__ row_slot, const int32_t* __restrict__ hist,
+                       const int32_t* __restrict__ first_blk) {
+  extern __shared__ int32_t aux_sh[];
+  const AuxSmem a = aux_smem(aux_sh, E);
+  const int c = blockIdx.x, warp = threadIdx.x >> 5;
+  const int per_warp = per_cta / kAuxWarps;
+  const int r0 = min(n, c * per_cta + warp * per_warp), r1 = min(n, r0 + per_warp);
+  aux_count(ids, r0, r1, E, a, nullptr);             // ids are inputs of the sort, not of the first launch
+  griddep_wait();                                    // the counting launch has completed
+  for (int e = threadIdx.x; e < E; e += kAuxThreads) {
+    int before = 0;
+    for (int g = 0; g < c; ++g) before += __ldcg(hist + static_cast<long long>(g) * E + e);
+    a.start[e] = __ldcg(first_blk + e) * bm + before;
+  }
+  __syncthreads();
+  aux_place(ids, r0, r1, E, topk, a, sorted_rows, sorted_tokens, row_slot);
+}
+
 static long long aux_ctas(long long n, int sms) {
-  long long g = (n + 2047) / 2048;
+  long long g = (n + kAuxRun - 1) / kAuxRun;
   if (g > sms) g = sms;
   return g < 1 ? 1 : g;
 }
 
 size_t moe_sort_aux_ws_bytes(int T, int topk, int E, int sms) {
-  return static_cast<size_t>(aux_ctas(static_cast<long long>(T) * topk, sms)) * E * sizeof(int32_t) + 256;
+  const long long g = aux_ctas(static_cast<long long>(T) * topk, sms);
+  return static_cast<size_t>(g + 1) * E * sizeof(int32_t) + 256;   // histograms, first blocks, ticket
 }
 
 int launch_moe_sort_aux(const int32_t* ids, int T, int topk, int E, int bm, int32_t* sorted_rows,
                         int32_t* block_expert, int32_t* num_blocks, int32_t* sorted_tokens, int32_t* row_slot,
                         void* ws, cudaStream_t st, int sms, unsigned long long wait_ns, unsigned int* status) {
+  (void)wait_ns;
+  (void)status;
   if (E > kAuxMaxExperts) return -1;
   const long long n = static_cast<long long>(T) * topk;
   const long long g = aux_ctas(n, sms);
-  // entries per CTA: a multiple of the 16 warps x 32 lanes
-  long long per = (n + g - 1) / g;
+  long long per = (n + g - 1) / g;                   // a multiple of the 16 warps x 32 lanes
   per = (per + kAuxThreads - 1) / kAuxThreads * kAuxThreads;
   if (per > kAuxMaxPerCta) return -1;
-  const size_t hist_bytes = static_cast<size_t>(g) * E * sizeof(int32_t);
-  unsigned int* bar = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + hist_bytes);
   const size_t shm = static_cast<size_t>((kAuxWarps * E + 1) / 2 + 3 * E + kAuxThreads) * sizeof(int32_t);
   static std::atomic<unsigned long long> attr_devs{0};
   if (ensure_func_attrs(attr_devs, [&] {
         const int max_shm = ((kAuxWarps * kAuxMaxExperts + 1) / 2 + 3 * kAuxMaxExperts + kAuxThreads) * 4;
-        return cudaFuncSetAttribute(moe_sort_aux_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_shm) ==
-               cudaSuccess;
+        return cudaFuncSetAttribute(moe_sort_aux_single, cudaFuncAttributeMaxDynamicSharedMemorySize, max_shm) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(moe_sort_aux_count, cudaFuncAttributeMaxDynamicSharedMemorySize, max_shm) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(moe_sort_aux_place, cudaFuncAttributeMaxDynamicSharedMemorySize, max_shm) ==
+                   cudaSuccess;
       }) != 0)
     return -4;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(g), 1, 1);
-  cfg.blockDim = dim3(kAuxThreads, 1, 1);
-  cfg.dynamicSmemBytes = shm;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;      // every CTA resident: the grid barrier cannot stall
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, moe_sort_aux_kernel, ids, static_cast<int>(n), topk, T, E, bm, static_cast<int>(per),
-                         sorted_rows, block_expert, num_blocks, sorted_tokens, row_slot,
-                         static_cast<int32_t*>(ws), bar, wait_ns, status) != cudaSuccess)
-    return -4;
+  auto launch = [&](auto kern, auto... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(g), 1, 1);
+    cfg.blockDim = dim3(kAuxThreads, 1, 1);
+    cfg.dynamicSmemBytes = shm;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? 0 : -4;
+  };
+  int rc;
+  if (n <= 32) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(32, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    rc = cudaLaunchKernelEx(&cfg, moe_sort_aux_warp, ids, static_cast<int>(n), topk, T, E, bm, sorted_rows,
+                            block_expert, num_blocks, sorted_tokens, row_slot) == cudaSuccess ? 0 : -4;
+  } else if (g == 1) {
+    rc = launch(moe_sort_aux_single, ids, static_cast<int>(n), topk, T, E, bm, sorted_rows, block_expert, num_blocks,
+                sorted_tokens, row_slot);
+  } else {
+    int32_t* hist = static_cast<int32_t*>(ws);
+    int32_t* first_blk = hist + g * E;
+    unsigned int* ticket = reinterpret_cast<unsigned int*>(first_blk + E);
+    rc = launch(moe_sort_aux_count, ids, static_cast<int>(n), T, E, bm, static_cast<int>(per), sorted_rows,
+                block_expert, num_blocks, sorted_tokens, hist, first_blk, ticket);
+    if (rc == 0)
+      rc = launch(moe_sort_aux_place, ids, static_cast<int>(n), topk, E, bm, static_cast<int>(per), sorted_rows,
+                  sorted_tokens, row_slot, static_cast<const int32_t*>(hist), static_cast<const int32_t*>(first_blk));
+  }
+  if (rc != 0) return rc;
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

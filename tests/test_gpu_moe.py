@@ -75,8 +75,8 @@ def run_sort_aux(ids, n_exp, bm, ws=None):
     return rows, bexp, nb, toks, slot, ws
 
 
-@pytest.mark.parametrize("T,n_exp,topk", [(1, E, TOPK), (16, E, TOPK), (256, E, TOPK), (4096, E, TOPK),
-                                          (37, 5, 3), (3000, 64, 8), (1, 4096, 1)])
+@pytest.mark.parametrize("T,n_exp,topk", [(1, E, TOPK), (2, E, TOPK), (3, E, TOPK), (16, E, TOPK), (256, E, TOPK),
+                                          (4096, E, TOPK), (37, 5, 3), (3000, 64, 8), (1, 4096, 1)])
 @pytest.mark.parametrize("bm", [16, 128])
 def test_sort_aux_bit_exact(T, n_exp, topk, bm):
     """The single-launch sort: sorted rows, block experts and block count equal
@@ -88,6 +88,26 @@ def test_sort_aux_bit_exact(T, n_exp, topk, bm):
     ws = None
     for _ in range(2):
         rows, bexp, nb, toks, slot, ws = run_sort_aux(ids, n_exp, bm, ws)
+        assert int(nb.item()) == enb
+        assert np.array_equal(rows.cpu().numpy()[:enb * bm], er)
+        assert np.array_equal(bexp.cpu().numpy()[:enb], ee)
+        assert np.array_equal(toks.cpu().numpy()[:enb * bm], et)
+        assert np.array_equal(slot.cpu().numpy(), es)
+
+
+@pytest.mark.parametrize("bm", [16, 32])
+def test_sort_aux_repeated_experts(bm):
+    """Rows that repeat an expert (more than a block's worth in the one-warp
+    path for up to 32 rows, and in the one-CTA path), and an expert id outside
+    [0, E) that is not routed."""
+    cases = [np.array([[3] * 20 + [1] * 5 + [3] * 7], dtype=np.int32),          # 32 rows, one token
+             np.array([[2, 2, 0], [2, 9, 1], [0, 2, 2]] * 13, dtype=np.int32)]   # 117 rows, id 9 >= E
+    for ids in cases:
+        T, topk = ids.shape
+        n_exp = 4 if ids.max() > 3 else 8
+        er, ee, enb = moe.sort_routed_rows(np.where(ids < n_exp, ids, -1), n_exp, bm)
+        rows, bexp, nb, toks, slot, _ = run_sort_aux(ids, n_exp, bm)
+        et, es = moe.sort_aux_arrays(er, T, topk)
         assert int(nb.item()) == enb
         assert np.array_equal(rows.cpu().numpy()[:enb * bm], er)
         assert np.array_equal(bexp.cpu().numpy()[:enb], ee)
