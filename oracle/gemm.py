@@ -13,6 +13,9 @@ Written out:
     abs[m, n]  = sum_k |a~[m, k] * w~[n, k]|          float64
     C[m, n]    = BF16_RNE(ref[m, n])
 
+gemm_a16w4 is the A16WFP4 variant (BF16 activations unquantised, same
+weights, same bound).
+
 Every product a~ * w~ is exact in float64 (3 significant bits each, exponents
 within range); the float64 sum (a library matmul) is within
 K * 2**-53 * abs of the exact value, far below the acceptance bound
@@ -65,6 +68,28 @@ def gemm_a4w4_entries(A_bits, W_bits, ms, ns):
     prod = a[im] * w[inn]
     ref = prod.sum(axis=1)
     abs_sum = np.abs(prod).sum(axis=1)
+    return ref, abs_sum, mxfp4.round_to_bf16_bits(ref)
+
+
+def gemm_a16w4(A_bits, W_bits):
+    """A16WFP4 GEMM: BF16 activations against MXFP4 weights.
+
+    "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Summary (the #4772
+    bullet): BF16 activation x decoded MXFP4 weight, BF16 out.  The
+    activations are used as they are (exact float64 values of the BF16
+    inputs); only the weights are quantised (oracle.mxfp4), then
+
+        ref[m, n] = sum_k a[m, k] * w~[n, k]       float64
+        abs[m, n] = sum_k |a[m, k] * w~[n, k]|     float64
+        C[m, n]   = BF16_RNE(ref[m, n])
+
+    A product of a BF16 value (8 significant bits) and a decoded E2M1 value (2)
+    is exact in float64.  Returns (ref, abs_sum, C_bits) like gemm_a4w4.
+    """
+    a = mxfp4.bf16_bits_to_f64(A_bits)
+    w = dequantized(W_bits)
+    ref = a @ w.T
+    abs_sum = np.abs(a) @ np.abs(w).T
     return ref, abs_sum, mxfp4.round_to_bf16_bits(ref)
 
 

@@ -139,3 +139,39 @@ def test_error_band_of_the_pages():
 def test_tolerance_formula():
     t = gemm.tolerance(np.array([-256.0, 0.0]), np.array([1024.0, 2.0 ** 20]))
     assert t[0] == 1.0 + 2.0 ** -10 and t[1] == 1.0
+
+
+def test_a16w4_matches_exact_rational_brute_force():
+    """A16WFP4: BF16 activations used exactly, MXFP4 weights (independent
+    quantiser), exact rational sums, BF16 rounding."""
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 5, 64
+    A = workloads.to_bf16_bits((rng.standard_normal((M, K)) * 3).astype(np.float32))
+    W = workloads.to_bf16_bits((rng.standard_normal((N, K)) * 0.1).astype(np.float32))
+    ref, abs_sum, cbits = gemm.gemm_a16w4(A, W)
+    for m in range(M):
+        a = [Fraction(bf16_value(v)) for v in A[m]]
+        for n in range(N):
+            w = brute_quant_row([bf16_value(v) for v in W[n]])
+            exact = sum(x * y for x, y in zip(a, w))
+            assert abs(Fraction(ref[m, n]) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
+            assert cbits[m, n] == exact_bf16_bits(exact)
+            assert abs(Fraction(abs_sum[m, n]) - sum(abs(x * y) for x, y in zip(a, w))) <= abs_sum[m, n] * 2 ** -50
+
+
+def test_a16w4_equals_a4w4_when_activations_are_on_the_grid():
+    """If every 32-block of A is already MXFP4-representable at the scale the
+    rule picks (quantisation is the identity), A16WFP4 and A4W4 agree; with
+    general A they differ (the activation quantisation is not skipped in A4W4)."""
+    rng = np.random.default_rng(12)
+    M, N, K = 4, 8, 128
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    vals = grid[rng.integers(0, 8, (M, K))] * np.where(rng.random((M, K)) < 0.5, -1.0, 1.0)
+    vals[:, ::32] = 6.0                       # block max 6 -> scale 2^0 keeps the grid values
+    A = workloads.to_bf16_bits(vals.astype(np.float32))
+    W = workloads.weight_bits(N, K)
+    r16, _, c16 = gemm.gemm_a16w4(A, W)
+    r4, _, c4 = gemm.gemm_a4w4(A, W)
+    assert np.array_equal(r16, r4) and np.array_equal(c16, c4)
+    A2 = workloads.activation_bits(M, K)
+    assert not np.allclose(gemm.gemm_a16w4(A2, W)[0], gemm.gemm_a4w4(A2, W)[0], rtol=1e-3)
