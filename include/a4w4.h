@@ -120,6 +120,19 @@ int a4w4_gemm_ex(const void* A_bf16, int M, int K, const void* Wq, const void* W
                  void* C_bf16, void* workspace, size_t ws_bytes, unsigned int flags, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* A16WFP4 GEMM:  C[M, N] (BF16) = A[M, K] (BF16, not quantised) x MXFP4(W)^T.
+ * "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Summary (the #4772
+ * bullet: BF16 activation x decoded MXFP4 weight).  Same arguments, layouts
+ * and shape contract as a4w4_gemm_ex with the same preshuffled Wq/Ws; no
+ * workspace.  Each weight tile is decoded to BF16 on chip (exact for E8M0
+ * scales from 2^-127 to 2^125, i.e. weight blocks whose largest magnitude is
+ * below 2^127) and multiplied in BF16 with fp32 accumulation; split-K is
+ * reduced inside thread-block clusters in a fixed order (deterministic).
+ * flags: A4W4_GEMM_WEIGHT_PREFETCH as for a4w4_gemm_ex. */
+int a4w4_gemm_a16w4(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
+                    void* C_bf16, unsigned int flags, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Standalone MXFP4 quantisation (plain layout).
  * "[gfx1250] Fuse A4W4 stage1 FP4 quantization", Summary (the standalone quant
  * kept as the fallback path).

@@ -21,6 +21,7 @@ from ._native import (  # noqa: F401
     a4w4_debug_gemm_export,
     a4w4_debug_moe_gemm1_export,
     a4w4_gemm,
+    a4w4_gemm_a16w4,
     a4w4_gemm_ex,
     a4w4_gemm_kernel_name,
     a4w4_gemm_noalloc,

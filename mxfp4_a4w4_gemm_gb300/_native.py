@@ -26,6 +26,7 @@ SIGNATURES = {
     "a4w4_workspace_init": (_c_int, [_vp, _c_size, _vp]),
     "a4w4_gemm": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, _vp]),
     "a4w4_gemm_ex": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, _vp, _c_size, ctypes.c_uint, _vp]),
+    "a4w4_gemm_a16w4": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _vp, ctypes.c_uint, _vp]),
     "a4w4_mxfp4_quant": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
     "a4w4_moe_w1_codes_bytes": (_c_size, [_c_int, _c_int, _c_int]),
     "a4w4_moe_w1_scales_bytes": (_c_size, [_c_int, _c_int, _c_int]),
@@ -155,6 +156,11 @@ def a4w4_gemm(A, M, K, Wq, Ws, N, C, workspace=None, ws_bytes=0, stream=None):
 def a4w4_gemm_ex(A, M, K, Wq, Ws, N, C, workspace=None, ws_bytes=0, flags=0, stream=None):
     _check("a4w4_gemm_ex", lib().a4w4_gemm_ex(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C), _ptr(workspace),
                                                ws_bytes, flags, _stream(stream)))
+
+
+def a4w4_gemm_a16w4(A, M, K, Wq, Ws, N, C, flags=0, stream=None):
+    _check("a4w4_gemm_a16w4", lib().a4w4_gemm_a16w4(_ptr(A), M, K, _ptr(Wq), _ptr(Ws), N, _ptr(C), flags,
+                                                    _stream(stream)))
 
 
 def a4w4_mxfp4_quant(X, rows, cols, q, scales, stream=None):

@@ -181,6 +181,21 @@ int a4w4_gemm(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, 
   return gemm_impl(A_bf16, M, K, Wq, Ws, N, C_bf16, workspace, ws_bytes, 0u, stream, a4w4::ActDump{});
 }
 
+int a4w4_gemm_a16w4(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N, void* C_bf16,
+                    unsigned int flags, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || N % 256 != 0 || K % 128 != 0) return A4W4_ERR_ARG;
+  if (!aligned16(A_bf16) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(C_bf16)) return A4W4_ERR_ARG;
+  if ((flags & ~static_cast<unsigned int>(A4W4_GEMM_WEIGHT_PREFETCH)) != 0) return A4W4_ERR_ARG;
+  const int sms = current_device_sms();
+  if (sms < 0) return sms;
+  unsigned int* status = status_ptr();
+  if (status == nullptr) return A4W4_ERR_LAUNCH;
+  const a4w4::GemmPlan plan = a4w4::plan_a16w4(M, N, K, sms);
+  return a4w4::launch_a16w4(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, as_stream(stream),
+                            g_wait_ns.load(std::memory_order_relaxed), status,
+                            (flags & A4W4_GEMM_WEIGHT_PREFETCH) ? 1 : 0);
+}
+
 int a4w4_mxfp4_quant(const void* X_bf16, int rows, int cols, void* q, void* scales, void* stream) {
   if (rows <= 0 || cols <= 0 || cols % 32 != 0) return A4W4_ERR_ARG;
   if (!aligned16(X_bf16) || !aligned16(q) || scales == nullptr) return A4W4_ERR_ARG;

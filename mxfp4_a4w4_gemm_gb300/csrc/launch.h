@@ -92,6 +92,11 @@ int launch_quant_activation_tiles(const void* a, int M, int K, void* aq, cudaStr
 int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                 void* C, void* ws, cudaStream_t st, unsigned long long wait_ns, unsigned int* status,
                 int prefetch_w, ActDump dump);
+// A16WFP4 (BF16 activations x MXFP4 weights): swap-AB tiles of 16 or 32
+// tokens, split-K reduced inside clusters; no workspace.
+GemmPlan plan_a16w4(int M, int N, int K, int sms);
+int launch_a16w4(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
+                 cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w);
 // plan.decode: the decode kernel (decode.cu); no workspace.
 int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                   void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w,
