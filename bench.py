@@ -520,11 +520,12 @@ def fp4_peak_tflops(peaks):
 
 def make_workload(name, args, dev):
     desc, shapes, family = WORKLOADS[name]
+    tokens = [int(t) for t in args.tokens.split(",")] if args.tokens else None
     if name == "moe":
-        return desc, MoeSweep(dev, inline=args.moe_inline)
+        return desc, MoeSweep(dev, tokens=tokens, inline=args.moe_inline)
     if name == "moe2":
-        return desc, Moe2Sweep(dev)
-    if args.shape and args.workload != "all":
+        return desc, Moe2Sweep(dev, tokens=tokens)
+    if args.shape and args.workload not in ("all", "moe", "moe2"):
         shapes = [tuple(int(v) for v in args.shape.split(","))]
         desc = f"one dense A4W4 GEMM {shapes[0][0]}x{shapes[0][1]}x{shapes[0][2]} ({name} inputs)"
     return desc, DenseSweep(shapes, family, dev, a16w4=(name == "a16w4"))
@@ -743,6 +744,33 @@ def e2e_pipelined(torch, stream, dev, wl, steps, barrier, world, run_step):
     return ({"value": round(job_throughput(world, wl.bytes_per_step, ms), 4), "unit": "TB/s",
              "ms_per_step": round(ms, 5), "h2d_bytes_per_step": wl.h2d_bytes,
              "d2h_bytes_per_step": wl.d2h_bytes}, steps + 4)
+
+
+def run_profile(args):
+    """A short eager run for profilers: the workload's set-up, then
+    args.steps steps of plain C ABI calls (no graphs, no spin-up, no
+    end-to-end or CPU legs), so that a profiler sees few, predictable
+    launches.  Prints one JSON line with the launches issued; not a bench
+    value."""
+    import torch
+    import mxfp4_a4w4_gemm_gb300 as a4w4
+    from mxfp4_a4w4_gemm_gb300 import build
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    a4w4.lib()
+    desc, wl = make_workload(args.workload, args, dev)
+    wl.flags = a4w4.A4W4_GEMM_WEIGHT_PREFETCH if args.weight_prefetch else 0
+    torch.cuda.synchronize()
+    for r in range(args.steps):
+        wl.step(r)
+    torch.cuda.synchronize()
+    status = a4w4.a4w4_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}: {a4w4.a4w4_strerror(status)}")
+    print(json.dumps({"profile": True, "workload": desc, "steps": args.steps,
+                      "launches": args.steps * wl.launches_per_step,
+                      "kernels": [wl.kernel_name(i) for i in range(len(wl.shapes))]}), flush=True)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -1045,6 +1073,9 @@ def main():
     ap.add_argument("--shape", default="", help="M,N,K: time one GEMM of the workload's input family "
                                                 "(with a single --workload)")
     ap.add_argument("--moe-inline", action="store_true", help="MoE: quantise gathered rows inline in every tile")
+    ap.add_argument("--tokens", default="", help="MoE workloads: comma-separated token counts (default all)")
+    ap.add_argument("--profile", action="store_true",
+                    help="a few eager steps for a profiler (no graphs, spin-up, e2e or CPU legs); not a bench value")
     ap.add_argument("--no-weight-prefetch", dest="weight_prefetch", action="store_false",
                     help="do not let a GEMM stream its weights before the previous kernel finishes (default: "
                          "it may, since the weights are prepared before the timed region and never written in it)")
@@ -1052,6 +1083,11 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local_rank = dist_env()
+    if args.profile:
+        if args.workload == "all":
+            ap.error("--profile needs a single --workload")
+        run_profile(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
