@@ -259,7 +259,7 @@ int a4w4_moe_gemm1_ex(const void* X_bf16, int T, int D, const int32_t* sorted_ro
  * Each routed row's product is scaled by its weight in fp32 and stored as an
  * fp32 row of the workspace ([T*topk, D], a4w4_moe_gemm2_workspace_bytes);
  * a second kernel adds a token's rows in k order (bitwise deterministic) and
- * rounds to BF16.  I % 256 == 0, D % 256 == 0. */
+ * rounds to BF16.  I % 256 == 0, I <= 1024, D % 256 == 0. */
 size_t a4w4_moe_gemm2_workspace_bytes(int T, int topk, int D);
 int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t* sorted_rows,
                    const int32_t* block_expert, const int32_t* num_blocks, int topk,

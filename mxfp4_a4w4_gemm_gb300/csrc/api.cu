@@ -312,7 +312,8 @@ int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t
                    const int32_t* block_expert, const int32_t* num_blocks, int topk, const float* topk_weights,
                    const void* W2q, const void* W2s, int E, int D, void* Y_bf16, void* ws, size_t ws_bytes,
                    void* stream) {
-  if (T <= 0 || I <= 0 || topk <= 0 || E <= 0 || D <= 0 || I % 256 != 0 || D % 256 != 0) return A4W4_ERR_ARG;
+  if (T <= 0 || I <= 0 || topk <= 0 || E <= 0 || D <= 0 || I % 256 != 0 || D % 256 != 0 || I > 1024)
+    return A4W4_ERR_ARG;
   if (static_cast<long long>(T) * topk > (1ll << 30)) return A4W4_ERR_ARG;
   if (!aligned16(A_q) || A_s == nullptr || !aligned16(W2q) || !aligned16(W2s) || !aligned16(Y_bf16) ||
       sorted_rows == nullptr || block_expert == nullptr || num_blocks == nullptr || topk_weights == nullptr ||
@@ -327,10 +328,17 @@ int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t
   if (status == nullptr) return A4W4_ERR_LAUNCH;
   const cudaStream_t st = as_stream(stream);
   float* partial = static_cast<float*>(ws);
-  const int rc = a4w4::launch_moe_gemm2(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, max_blocks, topk,
-                                        topk_weights, W2q, W2s, E, D, partial, st,
-                                        g_wait_ns.load(std::memory_order_relaxed), status);
-  if (rc != 0) return rc;
+  // Blocks of few valid rows (up to 32 routed rows per expert on average):
+  // the kernel that keeps a block's activation tiles resident over many
+  // column tiles; otherwise one CTA per (block, column tile).
+  const bool few_rows = static_cast<long long>(T) * topk <= 32ll * E;
+  const unsigned long long wait = g_wait_ns.load(std::memory_order_relaxed);
+  const int rc = few_rows ? a4w4::launch_moe_gemm2_resident(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks,
+                                                            max_blocks, topk, topk_weights, W2q, W2s, E, D, partial,
+                                                            st, wait, status, sms)
+                          : a4w4::launch_moe_gemm2(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, max_blocks,
+                                                   topk, topk_weights, W2q, W2s, E, D, partial, st, wait, status);
+  if (rc != 0) return rc == -1 ? A4W4_ERR_ARG : rc;
   return a4w4::launch_moe_sum(partial, T, topk, D, Y_bf16, st, sms);
 }
 

@@ -166,8 +166,10 @@ def run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb):
     return host_bits(Y)
 
 
-def test_gemm2_small_every_output():
-    T, E, topk, D, I = 21, 6, 3, 512, 256
+@pytest.mark.parametrize("T,E,topk", [(21, 6, 3),      # few rows per expert: resident-activation kernel
+                                       (200, 4, 2)])    # many: one CTA per (block, column tile)
+def test_gemm2_small_every_output(T, E, topk):
+    D, I = 512, 256
     ids = workloads.moe_topk_ids(T, E, topk)
     wts = workloads.moe_topk_weights(T, topk)
     H = workloads.moe_hidden_bits(T * topk, I)
