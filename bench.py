@@ -272,7 +272,7 @@ class DenseSweep:
     def kernel_name(self, i):
         M, N, K = self.shapes[i]
         if self.a16w4:
-            return f"a4w4_gemm_kernel<a16w4,{16 if M <= 16 else 32}>"
+            return f"a4w4_a16w4_kernel<{16 if M <= 16 else 32}>"
         return self.a4w4.a4w4_gemm_kernel_name(M, N, K)   # the library's own plan
 
     def launches_of(self, i):

@@ -5,7 +5,6 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 namespace a4w4 {
 
@@ -167,38 +166,6 @@ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t n, uint32_t sf_a, uint32
 // M / 16 at 24-28.
 __device__ __forceinline__ uint32_t idesc_bf16(uint32_t n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// 32 MXFP4 elements (one 16-byte chunk of packed E2M1 codes, element 2j in
-// the low nibble of byte j) with their E8M0 scale -> 16 words of packed BF16
-// pairs (element 2j in the low half of word j).  Exact: a decoded E2M1 value
-// times a power of two has at most two significant bits and, for scales
-// between 2^-127 and 2^125, lies within BF16's range (subnormals kept).
-__device__ __forceinline__ void decode_mxfp4x32_bf16(uint4 codes, uint32_t e8m0, uint32_t* out) {
-  const float sc = e8m0 ? __uint_as_float(e8m0 << 23) : __uint_as_float(0x00400000u);   // 2^(e8m0 - 127)
-  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      uint32_t h2;   // f16x2 of the byte's two E2M1 values: low nibble -> low half
-      asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}" : "=r"(h2) : "r"((w[q] >> (8 * b)) & 0xFFu));
-      const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))) * sc;
-      const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))) * sc;
-      uint32_t r;
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-      out[4 * q + b] = r;
-    }
-  }
 }
 
 // Copy a 128-row x 4-block scale atom (512 bytes, layout (r%32)*16+(r/32)*4+j)

@@ -35,10 +35,7 @@ namespace a4w4 {
 // once beforehand (plain MXFP4 layout) instead of quantising them per tile;
 // kMoe2: MoE GEMM2, GEMM1's output tiles (sorted-slot operand layout) streamed
 // by TMA against the expert's down projection, top-k weighted fp32 rows out.
-// kA16W4: A16WFP4, BF16 activations x MXFP4 weights; swap-AB orientation,
-// the producers decode each weight tile into a BF16 tile and stage the BF16
-// activations, tcgen05.mma.kind::f16.
-enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4, kMoe2 = 5, kA16W4 = 6 };
+enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4, kMoe2 = 5 };
 
 // MoE GEMM1 epilogue activation (a4w4.h: A4W4_MOE_ACT_*)
 constexpr int kActSwiglu = 0, kActSilu = 1;
@@ -81,8 +78,7 @@ constexpr int kMaxDecodeSplits = 16;  // decode kernel: non-portable clusters (a
 
 template <int MODE, int NX, int STAGES>
 struct Cfg {
-  static constexpr bool kSwapAB = MODE == kSwap || MODE == kA16W4;
-  static constexpr bool kBf16 = MODE == kA16W4;
+  static constexpr bool kSwapAB = MODE == kSwap;
   static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
@@ -93,32 +89,30 @@ struct Cfg {
   static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;  // MoE GEMM1
   static constexpr bool kRouted = kMoeAny || MODE == kMoe2;        // blocks of sorted routed rows
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
-  static constexpr int QWARPS = kBf16 ? 8 : (((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8);   // producer warps
+  static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer warps
   // epilogue warps (the first of the producer warps): MoE's SwiGLU + requant
   // epilogue splits each TMEM lane quadrant's columns over two warps
   static constexpr int EPI_WARPS = kMoeAny ? 8 : 4;
   static constexpr int EPI_THREADS = EPI_WARPS * 32;
   static constexpr int THREADS = 32 * (2 + QWARPS);
-  static constexpr int MIN_BLOCKS = kBf16 ? 1 : (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
+  static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
   static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
-  static constexpr int X_CODE_BYTES = kBf16 ? NX * 512 : NX * 128 + (kAInter ? 1024 : 0);   // BF16: 2 B per element
+  static constexpr int X_CODE_BYTES = NX * 128 + (kAInter ? 1024 : 0);
   static constexpr int W_SF_BYTES = W_ATOMS * 1024;
-  static constexpr int X_SF_BYTES = (kAInter || kBf16) ? 0 : 1024;
-  static constexpr int WB_BYTES = kBf16 ? 65536 : 0;             // decoded BF16 weight tile, 128 x 256
+  static constexpr int X_SF_BYTES = kAInter ? 0 : 1024;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_X = OFF_W + STAGES * W_CODE_BYTES;
   static constexpr int OFF_WSF = OFF_X + STAGES * X_CODE_BYTES;
   static constexpr int OFF_XSF = OFF_WSF + STAGES * W_SF_BYTES;
-  static constexpr int OFF_WB = OFF_XSF + STAGES * X_SF_BYTES;
   // swap-AB split-K: peers push fp32 partial slices here (owner-indexed slots)
   static constexpr int PUSH_BYTES = kSwapAB ? (NX + 8) * 512 : 0;
-  static constexpr int OFF_PUSH = OFF_WB + STAGES * WB_BYTES;
+  static constexpr int OFF_PUSH = OFF_XSF + STAGES * X_SF_BYTES;
   static constexpr int OFF_BAR = OFF_PUSH + PUSH_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (3 * STAGES + 1) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;       // + slack to align the base to 1024
   static constexpr int ACC_COLS = MMA_N;
-  static constexpr int SFA_COLS = kBf16 ? 0 : 8;                 // 2 K-atoms x 4 columns
-  static constexpr int SFB_COLS = kBf16 ? 0 : 8 * ((MMA_N + 127) / 128);
+  static constexpr int SFA_COLS = 8;                             // 2 K-atoms x 4 columns
+  static constexpr int SFB_COLS = 8 * ((MMA_N + 127) / 128);
   static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_NEED = ACC_COLS + STAGES * SF_STAGE_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512);
@@ -179,32 +173,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 24);
   volatile int* epi_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_w(s), 1);
-      mbar_init(full_x(s), Cf::QWARPS * 32);
-      mbar_init(empty(s), 1);
-    }
-    mbar_init(tmem_full, 1);
-    *abort_flag = 0;
-    *last_flag = 0;
-    *never = 0;
-    *epi_ready = 0;
-    fence_barrier_init();
-  }
-  // Activation rows that do not exist (beyond M, or padding of a routed
-  // block) are never written by the producers: their codes and scales are
-  // zeroed here once for every stage.
-  if (!Cf::kTmaA) {
-    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async_smem();
-  __syncthreads();                                 // barriers initialised
-  // Start streaming weights before TMEM allocation: the first ring pass needs
-  // no empty-slot wait (fresh barriers).
+  // The first ring pass needs no empty-slot wait (fresh barriers).
   const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
   const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
   // Dense large-M tiles re-read each weight tile from L2 once per activation
@@ -232,12 +201,41 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES, ws_e + watom * 1024, Cf::W_ATOMS * 1024, full_w(s), pol);
   };
   int issued = 0;
-  if (warp == 0 && lane == 0) {
-    // Weights are read before the grid dependency resolves only on request
-    // (the previous kernel on the stream must not write them), and never when
-    // a stage also carries activation tiles: those come from the kernel just
-    // before this one.
-    if (!p.prefetch_w || Cf::kTmaA) griddep_wait();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_w(s), 1);
+      mbar_init(full_x(s), Cf::QWARPS * 32);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *never = 0;
+    *epi_ready = 0;
+    fence_barrier_init();
+    if (p.prefetch_w && !Cf::kTmaA) {
+      // Prefetch: the first ring pass goes out before anything else the CTA
+      // sets up (a stage that also carries activation tiles never does:
+      // those come from the kernel just before this one).
+      issued = nk < STAGES ? nk : STAGES;
+      for (int i = 0; i < issued; ++i) issue_stage(i);
+    }
+  }
+  // Activation rows that do not exist (beyond M, or padding of a routed
+  // block) are never written by the producers: their codes and scales are
+  // zeroed here once for every stage.
+  if (!Cf::kTmaA) {
+    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();                                 // barriers initialised
+  if (warp == 0 && lane == 0 && !(p.prefetch_w && !Cf::kTmaA)) {
+    // Without prefetch the weights are read only once the grid dependency has
+    // resolved: the previous kernel on the stream may write them.
+    griddep_wait();
     issued = nk < STAGES ? nk : STAGES;
     for (int i = 0; i < issued; ++i) issue_stage(i);
   }
@@ -300,25 +298,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
           break;
         }
         tc_fence_after();
-        if constexpr (Cf::kBf16) {
-          // decoded BF16 weights (A operand, 4 atoms of 64 K) x BF16 tokens
-          // (B operand), K = 16 per instruction
-          const uint64_t wd = sdesc_sw128(base + Cf::OFF_WB + s * Cf::WB_BYTES);
-          const uint64_t xd = sdesc_sw128(base + Cf::OFF_X + s * Cf::X_CODE_BYTES);
-          const uint32_t idb = idesc_bf16(Cf::MMA_N);
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tmem, wd + ((g * 16384) >> 4) + kk * 2, xd + ((g * NX * 128) >> 4) + kk * 2, idb,
-                       (i > 0 || g > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(empty(s));
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-          continue;
-        }
         const uint32_t sfa = sf_col0 + s * Cf::SF_STAGE_COLS;
         const uint32_t sfb = sfa + Cf::SFA_COLS;
         const uint64_t ad = adesc0 + ((s * A_STAGE) >> 4), bd = bdesc0 + ((s * B_STAGE) >> 4);
@@ -356,56 +335,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     // ---------------- activation producers ----------------
     const int qt = threadIdx.x - 64;
     constexpr int P = Cf::QWARPS * 32;
-    if constexpr (Cf::kBf16) {
-      // Per stage: the BF16 activation chunks of the stage (NX rows x 32
-      // chunks of 8 elements; zeros beyond M or K) are loaded first, then,
-      // once the MXFP4 weight tile has landed, every thread decodes 4 of its
-      // 1024 16-byte code chunks (row r, 32-block c) into BF16 in the
-      // 128-byte-swizzled K-major tile (4 atoms of 64 K), stores its
-      // activation chunks the same way and arrives.
-      const int m0 = x_tile * NX;
-      constexpr int XCH = NX * 32 / P;
-      static_assert(NX * 32 % P == 0 && 1024 % P == 0, "producer split");
-      for (int i = 0; i < nk; ++i) {
-        const int s = i % STAGES;
-        if (!mbar_wait(empty(s), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        const int kbase = (kt0 + i) * 256;
-        uint4 xv[XCH];
-#pragma unroll
-        for (int u = 0; u < XCH; ++u) {
-          const int item = qt + u * P, n = item >> 5, c16 = item & 31, k = kbase + c16 * 8;
-          xv[u] = (m0 + n < p.M && k < p.K) ? ld_global_nc_v4(p.A + static_cast<long long>(m0 + n) * p.K + k)
-                                            : make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (!mbar_wait(full_w(s), (i / STAGES) & 1u, abort_flag, p.wait_ns, p.status)) break;
-        const uint8_t* wt = smem + Cf::OFF_W + s * Cf::W_CODE_BYTES;
-        const uint8_t* wsf = smem + Cf::OFF_WSF + s * Cf::W_SF_BYTES;
-        uint8_t* wb = smem + Cf::OFF_WB + s * Cf::WB_BYTES;
-#pragma unroll 1
-        for (int u = 0; u < 1024 / P; ++u) {
-          const int q = qt + u * P;
-          const int r = (q >> 6) * 8 + ((q >> 3) & 7), c = (q & 7) ^ (r & 7);
-          const uint4 code = *reinterpret_cast<const uint4*>(wt + q * 16);
-          const uint32_t e = wsf[(c >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (c & 3)];
-          uint32_t o[16];
-          decode_mxfp4x32_bf16(code, e, o);
-          uint8_t* row = wb + (c >> 1) * 16384 + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            *reinterpret_cast<uint4*>(row + ((((c & 1) * 4 + v) ^ (r & 7)) << 4)) =
-                make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-        }
-        uint8_t* xt = smem + Cf::OFF_X + s * Cf::X_CODE_BYTES;
-#pragma unroll
-        for (int u = 0; u < XCH; ++u) {
-          const int item = qt + u * P, n = item >> 5, c16 = item & 31;
-          *reinterpret_cast<uint4*>(xt + (c16 >> 3) * (NX * 128) + (n >> 3) * 1024 + (n & 7) * 128 +
-                                    (((c16 & 7) ^ (n & 7)) << 4)) = xv[u];
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(full_x(s));
-      }
-    } else {
     constexpr int PER = Cf::PER_THREAD;
     const uint16_t* rowp[PER];
     bool rvalid[PER];
@@ -566,8 +495,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         quant_stage(i, w);
       }
     }
-
-    }  // producers
 
     // ---------------- epilogue (4 warps, one per TMEM lane quadrant) ----------------
     if (warp < 2 + Cf::EPI_WARPS) {
@@ -1052,38 +979,6 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
     return launch_cfg<kPre, 128, 4>(a, grid, st);
   }
   return -4;   // every plan is one of the above
-}
-
-GemmPlan plan_a16w4(int M, int N, int K, int sms) {
-  GemmPlan pl{};
-  pl.kt = (K + 255) / 256;
-  pl.swap_ab = 1;
-  pl.nx = M <= 16 ? 16 : 32;
-  pl.w_tiles = N / 128;
-  pl.x_tiles = (M + pl.nx - 1) / pl.nx;
-  const int tiles = pl.w_tiles * pl.x_tiles;
-  int splits = sms / (tiles > 0 ? tiles : 1);       // one CTA per SM (its rings fill shared memory)
-  if (splits > pl.kt) splits = pl.kt;
-  if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
-  pl.splits = splits < 1 ? 1 : splits;
-  pl.cluster_reduce = pl.splits > 1;
-  return pl;
-}
-
-int launch_a16w4(const GemmPlan& pl, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
-                 cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w) {
-  GemmArgs a{};
-  a.prefetch_w = prefetch_w;
-  a.status = status;
-  a.A = static_cast<const uint16_t*>(A);
-  a.Wq = static_cast<const uint8_t*>(Wq);
-  a.Ws = static_cast<const uint8_t*>(Ws);
-  a.C = static_cast<uint16_t*>(C);
-  a.M = M; a.N = N; a.K = K; a.KT = pl.kt; a.splits = pl.splits; a.w_tiles = pl.w_tiles;
-  a.cluster_reduce = pl.cluster_reduce;
-  a.wait_ns = wait_ns;
-  const dim3 grid(pl.w_tiles, pl.x_tiles, pl.splits);
-  return pl.nx == 16 ? launch_cfg<kA16W4, 16, 2>(a, grid, st) : launch_cfg<kA16W4, 32, 2>(a, grid, st);
 }
 
 int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, const int32_t* block_expert,

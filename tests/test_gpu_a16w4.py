@@ -73,3 +73,16 @@ def test_a16w4_weight_prefetch_back_to_back():
     for (A, W), c in zip(problems, outs):
         ref, abs_sum, _ = gemm.gemm_a16w4(A, W)
         assert gemm_violations(c, ref, abs_sum)[0].size == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 256, 1024), (20, 512, 2304)])
+def test_a16w4_wide_scale_range(M, N, K):
+    """Weight blocks whose E8M0 scales span 2^-127 .. 2^124 (decoded weights
+    down to BF16 subnormals and up near BF16's largest binade), each against
+    activations of the reciprocal magnitude: every output within tolerance."""
+    A, W = workloads.wide_scale_problem(M, N, K)
+    c = run(A, W)
+    ref, abs_sum, _ = gemm.gemm_a16w4(A, W)
+    bad = gemm_violations(c, ref, abs_sum)
+    assert bad[0].size == 0, (f"{bad[0].size} of {c.size} outside tolerance, first (m, n) "
+                              f"{list(zip(bad[0][:5].tolist(), bad[1][:5].tolist()))}")

@@ -28,7 +28,7 @@ W_STD = 0.02
 OUTLIER_FRACTION = 0.01
 OUTLIER_GAIN = 20.0
 
-_TAG_A, _TAG_W, _TAG_X, _TAG_W1, _TAG_STRESS, _TAG_W2, _TAG_GATE, _TAG_H = 11, 12, 13, 14, 15, 16, 17, 18
+_TAG_A, _TAG_W, _TAG_X, _TAG_W1, _TAG_STRESS, _TAG_W2, _TAG_GATE, _TAG_H, _TAG_WIDE = 11, 12, 13, 14, 15, 16, 17, 18, 19
 
 
 def rng(*key):
@@ -119,6 +119,29 @@ def dense_problem(M, N, K, family, seed=0):
     else:
         A = activation_bits(M, K, seed)
     return A, weight_bits(N, K, seed)
+
+
+# K-block exponents of wide_scale_problem: both ends of the E8M0 range the
+# BF16-decoding paths cover, and points between.
+WIDE_EXPONENTS = (-126, -125, -124, -64, 0, 64, 124, 125)
+
+
+def wide_scale_problem(M, N, K, seed=6):
+    """(A_bits [M, K], W_bits [N, K]) whose 32-blocks of K span the weight
+    scale range: K-block b has weights +-U(0.5, 3) * 2**x and activations
+    +-U(0.5, 1.5) * 2**-x with x = WIDE_EXPONENTS[b % 8], so every product is
+    of order 1 while the weight blocks' E8M0 scales run from 2^-127 to about
+    2^124.  Activations stay BF16 normal numbers; the smallest weights are
+    BF16 subnormals."""
+    g = rng(seed, _TAG_WIDE, M, N, K)
+    nb = K // 32
+    x = np.array(WIDE_EXPONENTS, dtype=np.int64)[np.arange(nb) % len(WIDE_EXPONENTS)]
+    x = np.repeat(x, 32)
+    ws = np.where(g.random((N, K)) < 0.5, -1.0, 1.0)
+    as_ = np.where(g.random((M, K)) < 0.5, -1.0, 1.0)
+    w = ws * g.uniform(0.5, 3.0, (N, K)) * np.ldexp(1.0, x)[None, :]
+    a = as_ * g.uniform(0.5, 1.5, (M, K)) * np.ldexp(1.0, -x)[None, :]
+    return to_bf16_bits(a.astype(np.float32)), to_bf16_bits(w.astype(np.float32))
 
 
 def moe_topk_ids(T, E, topk, seed=2):
