@@ -184,15 +184,6 @@ __global__ void __launch_bounds__(HCfg<NX, SW>::THREADS, 1) a4w4_a16w4_kernel(co
   volatile int* epi_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 24);
   volatile int* owner_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
 
-  const uint64_t pol = policy_evict_first();   // every weight byte is read once
-  auto issue_w = [&](int i) {
-    const int s = i % SW;
-    const long long atom = weight_atom(w_tile, kt0 + i, p.KT);
-    mbar_arrive_expect_tx(full_w(s), Cf::W_STAGE + Cf::WSF_STAGE);
-    bulk_g2s(base + Cf::OFF_W + s * Cf::W_STAGE, p.Wq + atom * 16384, 16384, full_w(s), pol);
-    bulk_g2s(base + Cf::OFF_WSF + s * Cf::WSF_STAGE, p.Ws + atom * 1024, 1024, full_w(s), pol);
-  };
-  int issued = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
       mbar_init(full_w(s), 1);
@@ -208,12 +199,6 @@ __global__ void __launch_bounds__(HCfg<NX, SW>::THREADS, 1) a4w4_a16w4_kernel(co
     *never = 0;
     *epi_ready = 0;
     fence_barrier_init();
-    if (p.prefetch_w) {
-      // Prefetch: the first ring pass (no empty-slot waits) goes out before
-      // anything else the CTA sets up.
-      issued = nk < SW ? nk : SW;
-      for (int i = 0; i < issued; ++i) issue_w(i);
-    }
     if (p.splits > 1) {
       // this CTA's slice receives S x (its groups) x 16 bytes
       const int S = p.splits, G = mvalid * 32;
@@ -232,10 +217,20 @@ __global__ void __launch_bounds__(HCfg<NX, SW>::THREADS, 1) a4w4_a16w4_kernel(co
   if (p.splits > 1) cluster_arrive_relaxed();  // paired with cluster_wait() before the first push / the exit
   bool cluster_waited = false;
 
-  if (warp == 0 && lane == 0 && !p.prefetch_w) {
-    // Without prefetch the weights are read only once the grid dependency
-    // has resolved: the previous kernel on the stream may write them.
-    griddep_wait();
+  const uint64_t pol = policy_evict_first();   // every weight byte is read once
+  auto issue_w = [&](int i) {
+    const int s = i % SW;
+    const long long atom = weight_atom(w_tile, kt0 + i, p.KT);
+    mbar_arrive_expect_tx(full_w(s), Cf::W_STAGE + Cf::WSF_STAGE);
+    bulk_g2s(base + Cf::OFF_W + s * Cf::W_STAGE, p.Wq + atom * 16384, 16384, full_w(s), pol);
+    bulk_g2s(base + Cf::OFF_WSF + s * Cf::WSF_STAGE, p.Ws + atom * 1024, 1024, full_w(s), pol);
+  };
+  int issued = 0;
+  if (warp == 0 && lane == 0) {
+    // The first ring pass needs no empty-slot wait.  Weights are read before
+    // the grid dependency resolves only on request: the previous kernel on
+    // the stream must not write them.
+    if (!p.prefetch_w) griddep_wait();
     issued = nk < SW ? nk : SW;
     for (int i = 0; i < issued; ++i) issue_w(i);
   }

@@ -173,7 +173,32 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 24);
   volatile int* epi_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
 
-  // The first ring pass needs no empty-slot wait (fresh barriers).
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_w(s), 1);
+      mbar_init(full_x(s), Cf::QWARPS * 32);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *never = 0;
+    *epi_ready = 0;
+    fence_barrier_init();
+  }
+  // Activation rows that do not exist (beyond M, or padding of a routed
+  // block) are never written by the producers: their codes and scales are
+  // zeroed here once for every stage.
+  if (!Cf::kTmaA) {
+    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
+      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();                                 // barriers initialised
+  // Start streaming weights before TMEM allocation: the first ring pass needs
+  // no empty-slot wait (fresh barriers).
   const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
   const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
   // Dense large-M tiles re-read each weight tile from L2 once per activation
@@ -201,41 +226,12 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     bulk_g2s(base + Cf::OFF_WSF + s * Cf::W_SF_BYTES, ws_e + watom * 1024, Cf::W_ATOMS * 1024, full_w(s), pol);
   };
   int issued = 0;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_w(s), 1);
-      mbar_init(full_x(s), Cf::QWARPS * 32);
-      mbar_init(empty(s), 1);
-    }
-    mbar_init(tmem_full, 1);
-    *abort_flag = 0;
-    *last_flag = 0;
-    *never = 0;
-    *epi_ready = 0;
-    fence_barrier_init();
-    if (p.prefetch_w && !Cf::kTmaA) {
-      // Prefetch: the first ring pass goes out before anything else the CTA
-      // sets up (a stage that also carries activation tiles never does:
-      // those come from the kernel just before this one).
-      issued = nk < STAGES ? nk : STAGES;
-      for (int i = 0; i < issued; ++i) issue_stage(i);
-    }
-  }
-  // Activation rows that do not exist (beyond M, or padding of a routed
-  // block) are never written by the producers: their codes and scales are
-  // zeroed here once for every stage.
-  if (!Cf::kTmaA) {
-    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async_smem();
-  __syncthreads();                                 // barriers initialised
-  if (warp == 0 && lane == 0 && !(p.prefetch_w && !Cf::kTmaA)) {
-    // Without prefetch the weights are read only once the grid dependency has
-    // resolved: the previous kernel on the stream may write them.
-    griddep_wait();
+  if (warp == 0 && lane == 0) {
+    // Weights are read before the grid dependency resolves only on request
+    // (the previous kernel on the stream must not write them), and never when
+    // a stage also carries activation tiles: those come from the kernel just
+    // before this one.
+    if (!p.prefetch_w || Cf::kTmaA) griddep_wait();
     issued = nk < STAGES ? nk : STAGES;
     for (int i = 0; i < issued; ++i) issue_stage(i);
   }

@@ -41,7 +41,8 @@ def run(A_bits, W_bits, flags=0):
 
 CASES = [(1, 7168, 4224, "decode"), (8, 1536, 7168, "decode"), (32, 7168, 768, "decode"),
          (16, 256, 256, "small"), (17, 512, 1024, "large"), (40, 256, 384, "large"), (100, 1536, 4224, "large"),
-         (1, 256, 16384, "large"), (37, 1536, 4224, "stress"), (3, 2048, 2304, "decode")]
+         (1, 256, 16384, "large"), (37, 1536, 4224, "stress"), (3, 2048, 2304, "decode"),
+         (200, 512, 1024, "large"), (129, 256, 384, "stress")]
 
 
 @pytest.mark.parametrize("M,N,K,family", CASES, ids=[f"{f}-{m}x{n}x{k}" for m, n, k, f in CASES])
