@@ -87,3 +87,12 @@ def test_a16w4_wide_scale_range(M, N, K):
     bad = gemm_violations(c, ref, abs_sum)
     assert bad[0].size == 0, (f"{bad[0].size} of {c.size} outside tolerance, first (m, n) "
                               f"{list(zip(bad[0][:5].tolist(), bad[1][:5].tolist()))}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 7168, 4224), (32, 1536, 7168)])
+def test_a16w4_bitwise_deterministic(M, N, K):
+    """Split-K partials are summed in cluster-rank order: repeated runs agree bit for bit."""
+    A, W = workloads.dense_problem(M, N, K, "decode")
+    c1 = run(A, W)
+    c2 = run(A, W)
+    assert np.array_equal(c1, c2)

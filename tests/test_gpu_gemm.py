@@ -167,3 +167,19 @@ def test_weight_prefetch_back_to_back(M, N, K):
         c = C.cpu().numpy().view(np.uint16)
         bad = gemm_violations(c, ref, abs_sum)
         assert bad[0].size == 0, f"{bad[0].size} of {c.size} outside tolerance"
+
+
+@pytest.mark.parametrize("M,N,K,family", [
+    (1, 7168, 4224, "decode"),    # decode kernel: st.async split-K slices summed in rank order
+    (32, 7168, 4224, "decode"),   # swap-AB: cluster push, owner sums in split order
+    (200, 1536, 7168, "large"),   # quantise-once tiles, global split-K partials, last CTA sums
+    (513, 1536, 4224, "stress"),  # quantise-once tiles, cluster pull reduction
+], ids=lambda v: str(v))
+def test_bitwise_deterministic_per_plan(M, N, K, family):
+    """Every split-K reduction sums in a fixed order: three runs give the same bits."""
+    A, W = workloads.dense_problem(M, N, K, family)
+    prep = Prepared(W)
+    c1, ws = run_gemm(A, prep)
+    c2, _ = run_gemm(A, prep, ws)
+    c3, _ = run_gemm(A, prep)
+    assert np.array_equal(c1, c2) and np.array_equal(c2, c3)

@@ -248,3 +248,24 @@ def test_two_stages_chained(act):
     y, abs_sum, _ = moe.gemm2_tokens(out["codes"], out["scales"], p.ids, wts, lambda e: W2[e], np.nonzero(tok_ok)[0])
     bad = gemm_violations(y_gpu[tok_ok], y, abs_sum)[0]
     assert bad.size == 0, f"{bad.size} of {y.size} outputs outside tolerance"
+
+
+@pytest.mark.parametrize("T,E,topk", [(21, 6, 3), (200, 4, 2)])
+def test_gemm2_bitwise_deterministic(T, E, topk):
+    """Each routed row is written by one CTA and a token's rows are summed in k
+    order (both GEMM2 kernels): repeated runs agree bit for bit."""
+    D, I = 512, 256
+    ids = workloads.moe_topk_ids(T, E, topk)
+    wts = workloads.moe_topk_weights(T, topk)
+    q, s = mxfp4.mxfp4_quant(workloads.moe_hidden_bits(T * topk, I))
+    W2 = np.concatenate([workloads.moe_expert_w2_bits(e, D, I) for e in range(E)])
+    W2q = torch.empty(E * a4w4.a4w4_weight_codes_bytes(D, I), dtype=torch.uint8, device="cuda")
+    W2s = torch.empty(E * a4w4.a4w4_weight_scales_bytes(D, I), dtype=torch.uint8, device="cuda")
+    a4w4.a4w4_prepare_gemm_weight(dev_bits(W2), E * D, I, W2q, W2s)
+    rows, bexp, nb = run_sort(ids, E)
+    er, _, enb = moe.sort_routed_rows(ids, E, 128)
+    tq, ts = gemm2_tiles(q, s, er, enb, T * topk, I)
+    maxb = a4w4.a4w4_moe_max_blocks(T, topk, E, 128)
+    y1 = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
+    y2 = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
+    assert np.array_equal(y1, y2)
