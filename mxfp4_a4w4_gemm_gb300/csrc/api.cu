@@ -158,6 +158,8 @@ int a4w4_gemm_kernel_name(int M, int N, int K, char* buf, size_t n) {
   const a4w4::GemmPlan pl = a4w4::plan_gemm(M, N, K, sizing_sms());
   if (pl.decode)
     snprintf(buf, n, "a4w4_decode_kernel<%d,%d>", pl.nx, pl.ring);
+  else if (pl.persistent)
+    snprintf(buf, n, "a4w4_large_kernel<prequant,persistent>");
   else if (pl.prequant)
     snprintf(buf, n, "a4w4_gemm_kernel<prequant,%d>", pl.nx);
   else

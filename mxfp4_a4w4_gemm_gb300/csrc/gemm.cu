@@ -925,6 +925,14 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   if ((pl.swap_ab || M <= 128) && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   pl.splits = splits;
   pl.cluster_reduce = splits > 1 && splits <= kMaxClusterSplits;
+  if (pl.prequant && M > 128 && splits == 1) {
+    // At least one full wave of 128 x 256 tiles: one persistent CTA per SM
+    // walks them; a last wave of r tiles with 2r <= sms runs as 2r
+    // 128-column halves, so that it ends sooner.
+    pl.persistent = 1;
+    const int r = tiles % (sms > 0 ? sms : 1);
+    pl.half_tiles = (r > 0 && 2 * r <= sms) ? r : 0;
+  }
   // workspace: [activation tiles][fp32 split-K partials][tile counters]
   if (splits > 1 && !pl.cluster_reduce) {
     pl.partial_bytes = static_cast<size_t>(tiles) * splits * tile_elems * sizeof(float);
@@ -972,6 +980,7 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int rc = launch_quant_activation_tiles(A, M, K, const_cast<uint8_t*>(a.Aq), st, sms);
     if (rc != 0) return rc;
+    if (pl.persistent) return launch_large(pl, a.Aq, M, Wq, Ws, N, C, st, wait_ns, status, sms);
     return launch_cfg<kPre, 128, 4>(a, grid, st);
   }
   return -4;   // every plan is one of the above

@@ -1,0 +1,305 @@
+// large.cu -- persistent large-M dense A4W4 GEMM (sm_103a).
+//
+// "[gfx950][FlyDSL] Add direct dense A4W4 MXFP4 GEMM", Summary/Implementation
+// and the M = 1 ... 2048 microbenchmark: MXFP4 activations (quantised once
+// beforehand at large M, the page's separate-quant path) times preshuffled
+// MXFP4 weights, fp32 accumulation, BF16 output with M-tail masking.
+//
+// One CTA per SM walks a list of work units; a unit is a 128 x 256 output
+// tile (activation tile x, weight tile w), or one 128-column half of a tile of
+// the last, partial wave (two CTAs take the two halves: the wave's operand
+// bytes per SM drop from 51 KB to 34 KB per K step, its own output columns
+// each, nothing to reduce).  The operand ring runs on across units: the next
+// unit's copies land while the epilogue drains the accumulator.
+//   warp 0     producer: per 256-wide K step one 17 KB activation atom, the
+//              two adjacent 16 KB weight atoms and their 2 KB of scales (one
+//              atom and 1 KB for a half unit);
+//   warp 1     TMEM owner and MMA issuer: scale copies into TMEM, four
+//              tcgen05.mma.kind::mxf4.block_scale (M = 128, N = 256 or 128,
+//              K = 64) per step; before a unit's first MMA it waits until the
+//              epilogue has read the previous unit's accumulator;
+//   warps 2-5  epilogue (one per TMEM lane quadrant, a thread per row):
+//              TMEM -> BF16 in 64-column chunks, turned around in a small
+//              per-warp buffer so that each store writes whole 128-byte row
+//              segments; the accumulator is handed back as soon as its last
+//              columns are in registers.
+#include "device.cuh"
+#include "launch.h"
+
+namespace a4w4 {
+
+struct LargeArgs {
+  const uint8_t* Aq;        // activation tiles: atom (x_tile, kt) = 17408 bytes (codes, then scales)
+  const uint8_t* Wq;        // preshuffled weight codes
+  const uint8_t* Ws;        // preshuffled weight scales
+  uint16_t* C;              // [M, N] BF16
+  int M, N, KT, w_tiles;
+  int full_units;           // tiles 0 .. full_units-1 run whole
+  int units;                // full_units + 2 x (tiles run as two 128-column halves)
+  unsigned long long wait_ns;
+  unsigned int* status;
+};
+
+constexpr int kLargeStages = 4;
+
+struct LCfg {
+  static constexpr int STAGES = kLargeStages;
+  static constexpr int THREADS = 192;
+  static constexpr int A_BYTES = 17408;          // 128 rows x 256 K: codes + scales
+  static constexpr int W_BYTES = 32768;          // two 128-row weight atoms
+  static constexpr int WSF_BYTES = 2048;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_W = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_WSF = OFF_W + STAGES * W_BYTES;
+  // epilogue turnaround: per warp 32 rows x 64 BF16 columns, rows padded to
+  // 144 bytes (conflict-free 16-byte accesses row-wise and column-wise)
+  static constexpr int STG_PITCH = 144;
+  static constexpr int STG_BYTES = 32 * STG_PITCH;
+  static constexpr int OFF_STG = OFF_WSF + STAGES * WSF_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + 4 * STG_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 3;    // full, empty per stage; acc_full, acc_empty, drain
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
+  static constexpr int ACC_COLS = 256;
+  static constexpr int SFA_COLS = 8;             // 2 K halves x 4 columns
+  static constexpr int SFB_COLS = 16;            // 2 K halves x 2 weight atoms x 4 columns
+  static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(A_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "swizzled tiles start 1024-aligned");
+  static_assert(ACC_COLS + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Unit u -> tile and column half (-1: the whole 256 columns).
+__device__ __forceinline__ void large_unit(const LargeArgs& p, int u, int& tile, int& half) {
+  if (u < p.full_units) {
+    tile = u;
+    half = -1;
+  } else {
+    const int v = u - p.full_units;
+    tile = p.full_units + (v >> 1);
+    half = v & 1;
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const LargeArgs p) {
+  using Cf = LCfg;
+  constexpr int STAGES = Cf::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const unsigned long long drain_ns = p.wait_ns > 100000000ull ? p.wait_ns : 100000000ull;
+
+  const uint32_t bar0 = base + Cf::OFF_BAR;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);    // a unit's accumulator is complete
+  const uint32_t acc_empty = acc_full + 8u;               // the epilogue has read it
+  const uint32_t drain = acc_empty + 8u;                  // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cf::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 8);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 16);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cf::TMEM_COLS);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // The activation tiles come from the kernel just before this one.
+  griddep_wait();
+  griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();   // operands are re-read by other tiles from L2
+      int g = 0;                                  // stages issued (the ring runs on across units)
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += G) {
+        int tile, half;
+        large_unit(p, u, tile, half);
+        const int x_tile = tile / p.w_tiles, w_tile = tile % p.w_tiles;
+        const int atoms = half < 0 ? 2 : 1;
+        const uint32_t bytes = Cf::A_BYTES + atoms * (16384 + 1024);
+        for (int kt = 0; kt < p.KT; ++kt) {
+          const int s = g % STAGES;
+          if (!mbar_wait(empty(s), ((g / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          const long long aatom = static_cast<long long>(x_tile) * p.KT + kt;
+          const long long watom = weight_atom(2 * w_tile, kt, p.KT) + (half > 0 ? 1 : 0);
+          mbar_arrive_expect_tx(full(s), bytes);
+          bulk_g2s(base + Cf::OFF_A + s * Cf::A_BYTES, p.Aq + aatom * Cf::A_BYTES, Cf::A_BYTES, full(s), pol);
+          bulk_g2s(base + Cf::OFF_W + s * Cf::W_BYTES, p.Wq + watom * 16384, atoms * 16384, full(s), pol);
+          bulk_g2s(base + Cf::OFF_WSF + s * Cf::WSF_BYTES, p.Ws + watom * 1024, atoms * 1024, full(s), pol);
+          ++g;
+        }
+      }
+      // every copy issued lands before the CTA's shared memory is released
+      for (int j = (g > STAGES ? g - STAGES : 0); j < g; ++j)
+        mbar_wait(full(j % STAGES), (j / STAGES) & 1u, never, drain_ns, p.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint64_t adesc0 = sdesc_sw128(base + Cf::OFF_A), bdesc0 = sdesc_sw128(base + Cf::OFF_W);
+      const uint64_t asfd0 = sdesc_sf(base + Cf::OFF_A + 16384), bsfd0 = sdesc_sf(base + Cf::OFF_WSF);
+      const uint32_t id_full0 = idesc_mxf4(256, 0, 0), id_full2 = idesc_mxf4(256, 2, 2);
+      const uint32_t id_half0 = idesc_mxf4(128, 0, 0), id_half2 = idesc_mxf4(128, 2, 2);
+      const uint32_t sf_col0 = tmem + Cf::ACC_COLS;
+      int g = 0, j = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += G, ++j) {
+        int tile, half;
+        large_unit(p, u, tile, half);
+        // the epilogue has read the previous unit's accumulator
+        if (j > 0) {
+          if (!mbar_wait(acc_empty, static_cast<uint32_t>((j - 1) & 1), abort_flag, p.wait_ns, p.status)) break;
+          tc_fence_after();
+        }
+        const uint32_t idesc0 = half < 0 ? id_full0 : id_half0, idesc2 = half < 0 ? id_full2 : id_half2;
+        for (int kt = 0; kt < p.KT; ++kt) {
+          const int s = g % STAGES;
+          if (!mbar_wait(full(s), (g / STAGES) & 1u, abort_flag, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa = sf_col0 + s * Cf::SF_STAGE_COLS;
+          const uint32_t sfb = sfa + Cf::SFA_COLS;
+          const uint64_t ad = adesc0 + ((s * Cf::A_BYTES) >> 4), bd = bdesc0 + ((s * Cf::W_BYTES) >> 4);
+          const uint64_t asd = asfd0 + ((s * Cf::A_BYTES) >> 4), bsd = bsfd0 + ((s * Cf::WSF_BYTES) >> 4);
+#pragma unroll
+          for (int ka = 0; ka < 2; ++ka) {
+            tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
+            tmem_copy_sf_desc(sfb + ka * 8, bsd + (ka * 512) / 16);
+            if (half < 0) tmem_copy_sf_desc(sfb + ka * 8 + 4, bsd + (1024 + ka * 512) / 16);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const int ka = ks >> 1;
+            mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4, sfb + ka * 8,
+                     (kt > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(empty(s));
+          ++g;
+        }
+        if (ok) mma_commit(acc_full);
+      }
+      // TMEM is released only after every MMA issued has completed.
+      mma_commit(drain);
+      mbar_wait(drain, 0, never, drain_ns, p.status);
+    }
+  } else {
+    // ---------------- epilogue (4 warps, one per TMEM lane quadrant) ----------------
+    const int q = warp & 3;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint8_t* stg = smem + Cf::OFF_STG + (warp - 2) * Cf::STG_BYTES;
+    int j = 0;
+    for (int u = blockIdx.x; u < p.units; u += G, ++j) {
+      int tile, half;
+      large_unit(p, u, tile, half);
+      const int x_tile = tile / p.w_tiles, w_tile = tile % p.w_tiles;
+      if (!mbar_wait(acc_full, static_cast<uint32_t>(j & 1), abort_flag, p.wait_ns, p.status)) break;
+      __syncwarp();
+      tc_fence_after();
+      const int row0 = x_tile * 128 + q * 32;       // this warp's 32 rows
+      const int cols = half < 0 ? 256 : 128;
+      const int n0 = w_tile * 256 + (half > 0 ? 128 : 0);
+#pragma unroll 1
+      for (int c0 = 0; c0 < cols; c0 += 64) {
+        float v[64];
+        tmem_ld64(tq + c0, v);
+        if (c0 + 64 == cols) {
+          // the accumulator's last columns are in registers: the next unit's
+          // MMAs may overwrite it
+          tc_fence_before();
+          mbar_arrive(acc_empty);
+        }
+        // row lane -> buffer row; then 8 lanes per row, 4 rows per store
+        uint4* mine = reinterpret_cast<uint4*>(stg + lane * Cf::STG_PITCH);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          mine[t] = make_uint4(bf16x2_bits(v[8 * t], v[8 * t + 1]), bf16x2_bits(v[8 * t + 2], v[8 * t + 3]),
+                               bf16x2_bits(v[8 * t + 4], v[8 * t + 5]), bf16x2_bits(v[8 * t + 6], v[8 * t + 7]));
+        __syncwarp();
+#pragma unroll
+        for (int r4 = 0; r4 < 8; ++r4) {
+          const int r = r4 * 4 + (lane >> 3), seg = lane & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(stg + r * Cf::STG_PITCH + seg * 16);
+          if (row0 + r < p.M)
+            *reinterpret_cast<uint4*>(p.C + static_cast<long long>(row0 + r) * p.N + n0 + c0 + seg * 8) = val;
+        }
+        __syncwarp();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Cf::TMEM_COLS);
+  }
+}
+
+int launch_large(const GemmPlan& pl, const uint8_t* Aq, int M, const void* Wq, const void* Ws, int N, void* C,
+                 cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int sms) {
+  const int tiles = pl.x_tiles * pl.w_tiles;
+  const int units = tiles + pl.half_tiles;
+  if (tiles < 1 || pl.half_tiles < 0 || pl.half_tiles > tiles || sms < 1) return -4;
+  static std::atomic<unsigned long long> attr_devs{0};   // bit d: attribute set on device d
+  if (ensure_func_attrs(attr_devs, [&] {
+        return cudaFuncSetAttribute(a4w4_large_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    LCfg::SMEM_BYTES) == cudaSuccess;
+      }) != 0)
+    return -4;
+  LargeArgs a{};
+  a.Aq = Aq;
+  a.Wq = static_cast<const uint8_t*>(Wq);
+  a.Ws = static_cast<const uint8_t*>(Ws);
+  a.C = static_cast<uint16_t*>(C);
+  a.M = M; a.N = N; a.KT = pl.kt; a.w_tiles = pl.w_tiles;
+  a.full_units = tiles - pl.half_tiles;
+  a.units = units;
+  a.wait_ns = wait_ns;
+  a.status = status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units < sms ? units : sms, 1, 1);
+  cfg.blockDim = dim3(LCfg::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = LCfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, a4w4_large_kernel, a) != cudaSuccess) return -4;
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace a4w4

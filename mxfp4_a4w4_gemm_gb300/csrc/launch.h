@@ -14,6 +14,8 @@ struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
   int decode;       // 1: the decode kernel (decode.cu): M <= 16, and some M <= 32 (plan_gemm)
   int prequant;     // 1: activations quantised once into tiles first (large M)
+  int persistent;   // 1 (with prequant): the persistent large-M kernel (large.cu)
+  int half_tiles;   // persistent: tiles of the last partial wave run as two 128-column halves
   size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
   int w_tiles;      // weight-row tiles (N / 128 or N / 256)
@@ -97,6 +99,11 @@ int launch_gemm(const GemmPlan& plan, const void* A, int M, int K, const void* W
 GemmPlan plan_a16w4(int M, int N, int K, int sms);
 int launch_a16w4(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N, void* C,
                  cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w);
+// plan.persistent: one CTA per SM (at most `sms`) walking the 128 x 256 tiles
+// of the activation tiles already quantised into `Aq`, the last
+// plan.half_tiles of them as two 128-column halves each (large.cu).
+int launch_large(const GemmPlan& plan, const uint8_t* Aq, int M, const void* Wq, const void* Ws, int N, void* C,
+                 cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int sms);
 // plan.decode: the decode kernel (decode.cu); no workspace.
 int launch_decode(const GemmPlan& plan, const void* A, int M, int K, const void* Wq, const void* Ws, int N,
                   void* C, cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int prefetch_w,

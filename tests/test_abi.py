@@ -67,8 +67,10 @@ def test_kernel_routing_of_the_workload_shapes():
     assert name(1, 256, 16384 * 4) == "a4w4_decode_kernel<16,4>"    # a 3-deep ring would need > 16 splits
     assert name(37, 1536, 4224) == "a4w4_gemm_kernel<swap,64>"
     assert name(100, 1536, 4224) == "a4w4_gemm_kernel<swap,128>"     # N < 4096: swap-AB up to 128 tokens
-    for M in (128, 512, 2048):
-        assert name(M, 8448, 7168) == "a4w4_gemm_kernel<prequant,128>"
+    assert name(128, 8448, 7168) == "a4w4_gemm_kernel<prequant,128>"
+    for M in (512, 2048):                                              # 128 x 256 tiles fill the SMs
+        assert name(M, 8448, 7168) == "a4w4_large_kernel<prequant,persistent>"
+    assert name(513, 1536, 4224) == "a4w4_gemm_kernel<prequant,128>"  # 30 tiles: split-K instead
     with pytest.raises(a4w4.A4W4Error) as e:
         name(1, 300, 256)
     assert e.value.code == a4w4.A4W4_ERR_ARG

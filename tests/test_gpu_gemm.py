@@ -79,7 +79,10 @@ def test_ragged_m_spans_tiles(M):
                                    # decode kernel with 16 K splits filling the grid (uneven K ranges)
                                    (16, 1536, 7168), (17, 1536, 4224), (32, 512, 7168),
                                    # large-M tiles without split-K: one K tile; K range longer than the ring
-                                   (256, 512, 256), (1024, 5120, 1536)])
+                                   (256, 512, 256), (1024, 5120, 1536),
+                                   # persistent large-M walk: two tiles per CTA and a ragged last row
+                                   # tile; a last partial wave run as 128-column halves after a full tile
+                                   (1100, 8192, 512), (1200, 4096, 512)])
 def test_k_tails_and_shapes(M, N, K):
     A, W = workloads.dense_problem(M, N, K, "large", seed=K)
     check_full(A, W)
