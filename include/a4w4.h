@@ -83,21 +83,20 @@ int a4w4_prepare_gemm_weight(const void* W_bf16, int N, int K, void* Wq, void* W
  *   C_bf16 [M, N] row-major, rows >= M are never touched.
  *   M >= 1, N % 256 == 0, K % 128 == 0.
  * Small M uses weights-as-rows tiles (swap-AB) with split-K over the SMs,
- * reduced inside thread-block clusters (no workspace).  `workspace` holds,
- * where the plan needs them, the activations quantised once into tiles
- * (M > 128; M > 64 when N >= 4096) and fp32 split-K partial tiles + tile
- * counters (a tile split over more CTAs than one cluster holds).  It must
- * hold at least a4w4_gemm_workspace_bytes(M, N, K) bytes, zeroed once by
- * a4w4_workspace_init (the counters reset themselves after each call;
- * re-initialise after a TIMEOUT).  When that size is 0 the workspace may be NULL.  The reduction
+ * reduced inside thread-block clusters (no workspace).  Larger M (M > 128;
+ * M > 64 when N >= 4096) quantises the activations once into tiles, held in
+ * `workspace`, and runs whole 128 x 256 output tiles (no split-K).  The
+ * workspace must hold at least a4w4_gemm_workspace_bytes(M, N, K) bytes
+ * (a4w4_workspace_init may zero it; its contents are overwritten before they
+ * are read).  When that size is 0 the workspace may be NULL.  Every reduction
  * order is fixed, so results are bitwise deterministic. */
 size_t a4w4_gemm_workspace_bytes(int M, int N, int K);
 int a4w4_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 /* Name of the kernel instantiation a4w4_gemm(M, N, K) launches on the current
  * device (planned for GB300's 152 SMs when no device is visible), e.g.
  * "a4w4_decode_kernel<16,3>" (tokens per CTA, weight ring depth) or
- * "a4w4_gemm_kernel<swap,32>" / "a4w4_gemm_kernel<prequant,128>"; the
- * quantise-once plans also launch the activation pre-pass.  Host-only, no
+ * "a4w4_gemm_kernel<swap,32>" / "a4w4_large_kernel<prequant,persistent>";
+ * the quantise-once plans also launch the activation pre-pass.  Host-only, no
  * device work.  Writes a NUL-terminated string of at most n bytes (truncated)
  * into buf.  Returns A4W4_OK, or A4W4_ERR_ARG for a shape a4w4_gemm rejects,
  * a NULL buf or n == 0. */
@@ -275,20 +274,18 @@ int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t
  * owns all device memory, or a latency-critical path that cannot afford
  * cudaMalloc's implicit synchronisation -- and so cannot hand a4w4_gemm() the
  * workspace its plan needs for M > 64: the activations quantised once into
- * MXFP4 tiles (64 < M <= 128 when N >= 4096, every M > 128) and, for M > 128,
- * the fp32 split-K partial tiles and tile counters of a tile split over more
- * CTAs than one cluster holds.  M <= 64 uses no scratch.
+ * MXFP4 tiles (64 < M <= 128 when N >= 4096, every M > 128).  Smaller M uses
+ * no scratch.
  *   Scratch: a fixed 16 MiB array inside the library's device image.  It comes
  *   into being on a device with the first a4w4_gemm_noalloc call there (the
  *   CUDA runtime loads the library's device code lazily), which also looks up
  *   its device address, whatever the shape; make that first call before any
  *   stream capture.  It stays until the process exits.  No call allocates.
  *   A plan needing more than 16 MiB (a4w4_gemm_workspace_bytes(M, N, K) >
- *   16 MiB: at K = 7168, M above about 4,400 rows; or split-K partials such as
- *   those of 200 x 1536 x 7168, 18 MiB) is refused with A4W4_ERR_WORKSPACE.
- *   All calls on a GPU share the array and it keeps the last call's contents:
- *   each call clears the tile counters it uses on `stream` first, and calls
- *   that may run at the same time on one GPU (different streams) race on it --
+ *   16 MiB: at K = 7168, M above about 4,400 rows) is refused with
+ *   A4W4_ERR_WORKSPACE.  All calls on a GPU share the array and it keeps the
+ *   last call's contents (overwritten before they are read); calls that may
+ *   run at the same time on one GPU (different streams) race on it --
  *   serialise them. */
 int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const void* Ws, int N,
                       void* C_bf16, void* stream);

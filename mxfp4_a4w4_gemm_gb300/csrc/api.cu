@@ -160,8 +160,6 @@ int a4w4_gemm_kernel_name(int M, int N, int K, char* buf, size_t n) {
     snprintf(buf, n, "a4w4_decode_kernel<%d,%d>", pl.nx, pl.ring);
   else if (pl.persistent)
     snprintf(buf, n, "a4w4_large_kernel<prequant,persistent>");
-  else if (pl.prequant)
-    snprintf(buf, n, "a4w4_gemm_kernel<prequant,%d>", pl.nx);
   else
     snprintf(buf, n, "a4w4_gemm_kernel<swap,%d>", pl.nx);
   return A4W4_OK;

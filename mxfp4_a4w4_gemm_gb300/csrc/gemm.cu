@@ -27,28 +27,26 @@
 
 namespace a4w4 {
 
-// kSwap: weights x inline-quantised tokens (small M); kNormal: inline-quantised
-// rows x weights (the base of the MoE modes; dense GEMMs with M > 64 use kPre);
-// kMoe: kNormal over gathered sorted rows with the SwiGLU +
-// requant epilogue; kPre: rows quantised beforehand into tiles, both operands
-// streamed by TMA (large M); kMoePre: kMoe gathering rows that were quantised
-// once beforehand (plain MXFP4 layout) instead of quantising them per tile;
-// kMoe2: MoE GEMM2, GEMM1's output tiles (sorted-slot operand layout) streamed
-// by TMA against the expert's down projection, top-k weighted fp32 rows out.
-enum Mode { kSwap = 0, kNormal = 1, kMoe = 2, kPre = 3, kMoePre = 4, kMoe2 = 5 };
+// kSwap: weights x inline-quantised tokens (17 <= M <= 128; larger M runs in
+// the persistent kernel of large.cu); kMoe: inline-quantised gathered sorted
+// rows x an expert's weights with the SwiGLU / SiLU + requant epilogue;
+// kMoePre: kMoe gathering rows that were quantised once beforehand (plain
+// MXFP4 layout) instead of quantising them per tile; kMoe2: MoE GEMM2, GEMM1's
+// output tiles (sorted-slot operand layout) streamed by TMA against the
+// expert's down projection, top-k weighted fp32 rows out.
+enum Mode { kSwap = 0, kMoe = 1, kMoePre = 2, kMoe2 = 3 };
 
 // MoE GEMM1 epilogue activation (a4w4.h: A4W4_MOE_ACT_*)
 constexpr int kActSwiglu = 0, kActSilu = 1;
 
 struct GemmArgs {
   const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
-  const uint8_t* Aq;  // kPre: activation tiles (weight layout), codes
-  const uint8_t* As;  // kPre: activation tiles, scales
+  const uint8_t* Aq;  // kMoe2: activation tiles (weight layout), codes; kMoePre: MXFP4 rows
+  const uint8_t* As;  // kMoe2: activation tiles, scales; kMoePre: E8M0 rows
   const uint8_t* Wq;
   const uint8_t* Ws;
   uint16_t* C;        // [M, N] BF16
-  float* partial;
-  unsigned int* counters;
+  float* partial;        // kMoe2: [T*topk, D] fp32 weighted rows
   int M, N, K, KT, splits, w_tiles;
   int cluster_reduce;   // 1: the `splits` CTAs of a tile form a cluster and reduce over DSMEM
   int prefetch_w;       // 1: weights may be read before the previous grid on the stream completes
@@ -72,7 +70,6 @@ struct GemmArgs {
   uint8_t* dump_scales;
 };
 
-constexpr int kRedStride = 260;      // floats per staged row of a 128x256 partial (1040 bytes)
 constexpr int kMaxClusterSplits = 8;  // portable cluster size
 constexpr int kMaxDecodeSplits = 16;  // decode kernel: non-portable clusters (a GPC holds at least 16 SMs)
 
@@ -82,10 +79,7 @@ struct Cfg {
   static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
-  static constexpr bool kTmaA = MODE == kPre || MODE == kMoe2;   // activations arrive by TMA too
-  // kPre's activation tiles (written by the pre-pass) hold each atom's codes
-  // and scales in one 17 KB block: one bulk copy per stage
-  static constexpr bool kAInter = MODE == kPre;
+  static constexpr bool kTmaA = MODE == kMoe2;                  // activations arrive by TMA too
   static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;  // MoE GEMM1
   static constexpr bool kRouted = kMoeAny || MODE == kMoe2;        // blocks of sorted routed rows
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
@@ -97,9 +91,9 @@ struct Cfg {
   static constexpr int THREADS = 32 * (2 + QWARPS);
   static constexpr int MIN_BLOCKS = (kSwapAB && NX <= 16) ? 3 : (kSwapAB && NX <= 32) ? 2 : 1;
   static constexpr int W_CODE_BYTES = W_ATOMS * 16384;
-  static constexpr int X_CODE_BYTES = NX * 128 + (kAInter ? 1024 : 0);
+  static constexpr int X_CODE_BYTES = NX * 128;
   static constexpr int W_SF_BYTES = W_ATOMS * 1024;
-  static constexpr int X_SF_BYTES = kAInter ? 0 : 1024;
+  static constexpr int X_SF_BYTES = 1024;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_X = OFF_W + STAGES * W_CODE_BYTES;
   static constexpr int OFF_WSF = OFF_X + STAGES * X_CODE_BYTES;
@@ -124,14 +118,8 @@ struct Cfg {
   static_assert(MIN_BLOCKS * TMEM_COLS <= 512, "co-resident CTAs must fit in TMEM");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024) <= 233472, "co-resident CTAs must fit in shared memory");
-  static constexpr int RED_BYTES = kSwapAB ? NX * 128 * 4 : 128 * kRedStride * 4;
-  static_assert(RED_BYTES <= OFF_PUSH, "a staged split-K partial must fit in the drained ring");
+  static_assert(!kSwapAB || NX * 128 * 4 <= OFF_PUSH, "a staged split-K partial must fit in the drained ring");
 };
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 template <int MODE, int NX, int STAGES>
 __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, STAGES>::MIN_BLOCKS)
@@ -169,7 +157,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   const uint32_t tmem_full = bar0 + 8u * (3 * STAGES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cf::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 8);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 16);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 24);
   volatile int* epi_ready = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 28);
 
@@ -181,7 +168,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
     mbar_init(tmem_full, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     *never = 0;
     *epi_ready = 0;
     fence_barrier_init();
@@ -201,23 +187,18 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   // no empty-slot wait (fresh barriers).
   const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
   const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
-  // Dense large-M tiles re-read each weight tile from L2 once per activation
-  // tile (evict-last); swap-AB and MoE GEMM1 stream every weight byte once.
-  // MoE GEMM2 reads each block's activation tiles once per output-column
-  // tile (evict-last) and the expert's weights about once (evict-first).
-  const uint64_t pol = (MODE == kNormal || MODE == kPre) ? policy_evict_last() : policy_evict_first();
+  // Swap-AB and MoE GEMM1 stream every weight byte once.  MoE GEMM2 reads
+  // each block's activation tiles once per output-column tile (evict-last)
+  // and the expert's weights about once (evict-first).
+  const uint64_t pol = policy_evict_first();
   const uint64_t pol_a = Cf::kTmaA ? policy_evict_last() : pol;
   auto issue_stage = [&](int i) {
     const int s = i % STAGES;
     mbar_arrive_expect_tx(full_w(s), (Cf::W_ATOMS + (Cf::kTmaA ? 1 : 0)) * (16384 + 1024));
     if (Cf::kTmaA) {
       const long long atom = static_cast<long long>(x_tile) * p.KT + (kt0 + i);
-      if (Cf::kAInter) {
-        bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 17408, 17408, full_w(s), pol_a);
-      } else {
-        bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
-        bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
-      }
+      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
+      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
     }
     // the W_ATOMS atoms of this K tile are adjacent (weight_atom): one copy
     // of codes, one of scales
@@ -275,11 +256,11 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       bool ok = true;
       const uint32_t a_tile0 = base + (Cf::kSwapAB ? Cf::OFF_W : Cf::OFF_X);
       const uint32_t b_tile0 = base + (Cf::kSwapAB ? Cf::OFF_X : Cf::OFF_W);
-      const uint32_t a_sf0 = base + (Cf::kSwapAB ? Cf::OFF_WSF : (Cf::kAInter ? Cf::OFF_X + 16384 : Cf::OFF_XSF));
+      const uint32_t a_sf0 = base + (Cf::kSwapAB ? Cf::OFF_WSF : Cf::OFF_XSF);
       const uint32_t b_sf0 = base + (Cf::kSwapAB ? Cf::OFF_XSF : Cf::OFF_WSF);
       constexpr uint32_t A_STAGE = Cf::kSwapAB ? Cf::W_CODE_BYTES : Cf::X_CODE_BYTES;
       constexpr uint32_t B_STAGE = Cf::kSwapAB ? Cf::X_CODE_BYTES : Cf::W_CODE_BYTES;
-      constexpr uint32_t ASF_STAGE = Cf::kSwapAB ? Cf::W_SF_BYTES : (Cf::kAInter ? Cf::X_CODE_BYTES : Cf::X_SF_BYTES);
+      constexpr uint32_t ASF_STAGE = Cf::kSwapAB ? Cf::W_SF_BYTES : Cf::X_SF_BYTES;
       constexpr uint32_t BSF_STAGE = Cf::kSwapAB ? Cf::X_SF_BYTES : Cf::W_SF_BYTES;
       const uint64_t adesc0 = sdesc_sw128(a_tile0), bdesc0 = sdesc_sw128(b_tile0);
       const uint64_t asfd0 = sdesc_sf(a_sf0), bsfd0 = sdesc_sf(b_sf0);
@@ -549,111 +530,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
               for (int i = et; i < n4; i += 128)
                 st_shared_cluster_v4(cluster_map_shared(slot + static_cast<uint32_t>(i * 16), static_cast<uint32_t>(o)), src[i]);
             }
-          } else {
-            const int tile = x_tile * p.w_tiles + w_tile;
-            float* part = p.partial + (static_cast<long long>(tile) * p.splits + split) * (128 * NX);
-#pragma unroll
-            for (int c0 = 0; c0 < NX; c0 += 16) {
-              float v[16];
-              tmem_ld16(tq + c0, v);
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (c0 + j < mvalid) __stcg(part + (c0 + j) * 128 + lrow, v[j]);
-            }
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (warp == 2 && lane == 0) {
-              const unsigned prev = atomicAdd(p.counters + tile, 1u);
-              *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
-            }
-            named_bar_sync(1, 128);
-            if (*last_flag) {
-              __threadfence();
-              const float* tbase = p.partial + static_cast<long long>(tile) * p.splits * (128 * NX);
-              for (int t = 0; t < mvalid; ++t) {
-                float acc = 0.f;
-                for (int sp = 0; sp < p.splits; ++sp) acc += __ldcg(tbase + static_cast<long long>(sp) * (128 * NX) + t * 128 + lrow);
-                p.C[static_cast<long long>(m0 + t) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-              }
-              if (warp == 2 && lane == 0) p.counters[tile] = 0u;
-            }
-          }
-        } else if (MODE == kNormal || MODE == kPre) {
-          const int m = x_tile * 128 + lrow;
-          const int n0 = w_tile * 256;
-          if (p.splits == 1) {
-            // Each thread stages its BF16 row in the drained ring (pitch 528
-            // bytes, so that a warp's row-parallel 16-byte stores spread over
-            // the banks) and writes it with one 512-byte bulk store, waiting
-            // until the store has read the row before the CTA may release the
-            // shared memory.
-            constexpr int kRowPitch = 528;
-            uint8_t* my = smem + lrow * kRowPitch;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 256; c0 += 64) {
-              float v[64];
-              tmem_ld64(tq + c0, v);
-              uint4* d = reinterpret_cast<uint4*>(my + c0 * 2);
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                d[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-            }
-            fence_proxy_async_smem();
-            if (m < p.M) {
-              bulk_s2g(p.C + static_cast<long long>(m) * p.N + n0, base + static_cast<uint32_t>(lrow * kRowPitch), 512);
-              bulk_commit_wait_read();
-            }
-          } else if (p.cluster_reduce) {
-            // fp32 partial [row][col] into this CTA's (drained) ring, rows padded
-            // to 260 floats so that the warp's row-parallel stores spread over banks
-            float* red = reinterpret_cast<float*>(smem);
-#pragma unroll 4
-            for (int c0 = 0; c0 < 256; c0 += 16) {
-              float v[16];
-              tmem_ld16(tq + c0, v);
-              if (m < p.M) {                       // rows beyond M are never read
-                float4* dst = reinterpret_cast<float4*>(red + lrow * kRedStride + c0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-              }
-            }
-          } else {
-            const int tile = x_tile * p.w_tiles + w_tile;
-            float* part = p.partial + (static_cast<long long>(tile) * p.splits + split) * (128 * 256);
-#pragma unroll 4
-            for (int c0 = 0; c0 < 256; c0 += 16) {
-              float v[16];
-              tmem_ld16(tq + c0, v);
-              float4* dst = reinterpret_cast<float4*>(part + lrow * 256 + c0);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) __stcg(dst + j, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            }
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (warp == 2 && lane == 0) {
-              const unsigned prev = atomicAdd(p.counters + tile, 1u);
-              *last_flag = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
-            }
-            named_bar_sync(1, 128);
-            if (*last_flag) {
-              __threadfence();
-              const float* tbase = p.partial + static_cast<long long>(tile) * p.splits * (128 * 256);
-              if (m < p.M) {
-                for (int c0 = 0; c0 < 256; c0 += 8) {
-                  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                  for (int sp = 0; sp < p.splits; ++sp) {
-                    const float4* src = reinterpret_cast<const float4*>(tbase + static_cast<long long>(sp) * (128 * 256) + lrow * 256 + c0);
-                    const float4 a = __ldcg(src), b = __ldcg(src + 1);
-                    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-                  }
-                  *reinterpret_cast<uint4*>(p.C + static_cast<long long>(m) * p.N + n0 + c0) =
-                      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-                }
-              }
-              if (warp == 2 && lane == 0) p.counters[tile] = 0u;
-            }
           }
         } else if (MODE == kMoe2) {
           // MoE GEMM2: each valid sorted slot's fp32 row (256 output columns)
@@ -730,74 +606,30 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     }
   }
 
-  if (!Cf::kMoeAny && p.cluster_reduce) {
-    // Split-K over the cluster: every CTA has parked its fp32 partial in its
-    // own shared memory; CTA `rank` sums a disjoint slice of the tile from all
-    // peers in split order (bitwise deterministic) and writes BF16.  Every
-    // thread of every CTA reaches both cluster barriers.
+  if (Cf::kSwapAB && p.cluster_reduce) {
+    // Split-K over the cluster: every CTA has pushed its slices of the fp32
+    // partial into their owners' push buffers; CTA `rank` owns tokens
+    // [rank*U, rank*U + U) and sums the pushed slots locally in split order
+    // (bitwise deterministic).  Every thread of every CTA reaches the cluster
+    // barrier, so that all pushes have landed.
     cluster_sync_all();
     if (warp >= 2 && warp < 6) {
       const int et = threadIdx.x - 64;
       const int S = p.splits;
       const uint32_t rank = cluster_ctarank();
-      const uint32_t red = smem_u32(smem);
-      if (Cf::kSwapAB) {
-        // this CTA owns tokens [rank*U, rank*U + U): sum the pushed slots
-        // locally in split order
-        const int m0 = x_tile * NX;
-        const int mvalid = min(NX, p.M - m0);
-        const int n = w_tile * 128 + et;
-        const int U = (NX + S - 1) / S;
-        const float* push = reinterpret_cast<const float*>(smem + Cf::OFF_PUSH);
-        const int t0 = static_cast<int>(rank) * U;
-        const int t1 = min(t0 + U, mvalid);
-        for (int t = t0; t < t1; ++t) {
-          float acc = 0.f;
-          for (int c = 0; c < S; ++c) acc += push[(c * U + (t - t0)) * 128 + et];
-          p.C[static_cast<long long>(m0 + t) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-        }
-      } else {
-        const int m0 = x_tile * 128;
-        const int rvalid = min(128, p.M - m0);
-        // this CTA owns rows rank, rank + S, ...: thread et sums 4 columns
-        // (16-byte remote loads) of every second of them, four rows in flight
-        // at once (remote loads are slow one at a time, fast together)
-        const int cq = et & 63, rsub = et >> 6;
-        const int n = w_tile * 256 + 4 * cq;
-        for (int j0 = 0;; j0 += 4) {
-          float4 acc[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            const int r = static_cast<int>(rank) + S * (rsub + 2 * (j0 + u));
-            if (r < rvalid) {
-              const uint32_t off = red + static_cast<uint32_t>((r * kRedStride + 4 * cq) * 4);
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                if (c < S) {
-                  const float4 v = ld_shared_cluster_f32x4(cluster_map_shared(off, c));
-                  acc[u].x += v.x;
-                  acc[u].y += v.y;
-                  acc[u].z += v.z;
-                  acc[u].w += v.w;
-                }
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int r = static_cast<int>(rank) + S * (rsub + 2 * (j0 + u));
-            if (r < rvalid)
-              *reinterpret_cast<uint2*>(p.C + static_cast<long long>(m0 + r) * p.N + n) =
-                  make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
-          }
-          if (static_cast<int>(rank) + S * (rsub + 2 * (j0 + 4)) >= rvalid &&
-              static_cast<int>(rank) + S * (2 * (j0 + 4)) >= rvalid)
-            break;
-        }
+      const int m0 = x_tile * NX;
+      const int mvalid = min(NX, p.M - m0);
+      const int n = w_tile * 128 + et;
+      const int U = (NX + S - 1) / S;
+      const float* push = reinterpret_cast<const float*>(smem + Cf::OFF_PUSH);
+      const int t0 = static_cast<int>(rank) * U;
+      const int t1 = min(t0 + U, mvalid);
+      for (int t = t0; t < t1; ++t) {
+        float acc = 0.f;
+        for (int c = 0; c < S; ++c) acc += push[(c * U + (t - t0)) * 128 + et];
+        p.C[static_cast<long long>(m0 + t) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
       }
     }
-    // pull mode: no CTA leaves while a peer may still read its shared memory
-    if (!Cf::kSwapAB) cluster_sync_all();
   }
 
   tc_fence_before();
@@ -862,25 +694,39 @@ static int decode_splits(int kt, int ring, int w_tiles, int sms) {
   return splits < 1 ? 1 : splits;
 }
 
+// Quantise-once plans (M > 128, or M > 64 with N >= 4096): the persistent
+// large-M kernel (large.cu) walks the 128 x 256 tiles, one CTA per SM; a last
+// wave of r < sms tiles with 2r <= sms (every tile, when they are that few)
+// runs as 2r 128-column halves.  No split-K: the activation tiles are the
+// whole workspace.
+static void plan_persistent(GemmPlan& pl, int M, int N, int sms) {
+  pl.swap_ab = 0;
+  pl.prequant = 1;
+  pl.persistent = 1;
+  pl.nx = 128;
+  pl.w_tiles = N / 256;
+  pl.x_tiles = (M + 127) / 128;
+  pl.splits = 1;
+  const int tiles = pl.w_tiles * pl.x_tiles;
+  const int r = tiles % (sms > 0 ? sms : 1);
+  pl.half_tiles = (r > 0 && 2 * r <= sms) ? r : 0;
+  pl.aq_bytes = static_cast<size_t>(pl.x_tiles) * pl.kt * (16384 + 1024);
+  pl.ws_bytes = pl.aq_bytes;
+}
+
 GemmPlan plan_gemm(int M, int N, int K, int sms) {
   GemmPlan pl{};
   pl.kt = (K + 255) / 256;
-  int ctas_per_sm;
-  size_t tile_elems;
-  if (M > 64 && M <= 128 && N / 256 >= 16) {
-    // tokens on the MMA's 128-row side, weights on N = 256: fewer operand
-    // bytes per weight byte than swap-AB once M passes 64.  The activations
-    // are quantised once into a tile (every weight tile's CTA would otherwise
-    // load the same BF16 rows, 4x the bytes of their MXFP4 codes).
-    pl.swap_ab = 0;
-    pl.prequant = 1;
-    pl.nx = 128;
-    pl.w_tiles = N / 256;
-    pl.x_tiles = 1;
-    pl.aq_bytes = static_cast<size_t>(pl.kt) * (16384 + 1024);
-    ctas_per_sm = 1;
-    tile_elems = static_cast<size_t>(128) * 256;
-  } else if (M <= 16 || (M <= 32 && (pl.kt <= 4 || decode_splits(pl.kt, 4, N / 128, sms) > kMaxClusterSplits))) {
+  if (M > 128 || (M > 64 && N / 256 >= 16)) {
+    // 128 x 256 tiles with the tokens on the MMA's 128-row side: fewer
+    // operand bytes per weight byte than swap-AB once M passes 64 (for N <
+    // 4096, swap-AB's split-K spreads the few tiles better up to 128 rows).
+    // The activations are quantised once into tiles (every weight tile's CTA
+    // would otherwise load the same BF16 rows, 4x the bytes of their codes).
+    plan_persistent(pl, M, N, sms);
+    return pl;
+  }
+  if (M <= 16 || (M <= 32 && (pl.kt <= 4 || decode_splits(pl.kt, 4, N / 128, sms) > kMaxClusterSplits))) {
     // Decode kernel (decode.cu), no workspace.  16 tokens: 3 CTAs fit per SM,
     // so a 3-deep ring (room for the next grid's CTAs to start early and
     // stream their weights), 4 deep when 3 would need over 16 splits.  32
@@ -897,48 +743,21 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
     pl.splits = decode_splits(pl.kt, pl.ring, pl.w_tiles, sms);
     pl.cluster_reduce = pl.splits > 1;
     return pl;
-  } else if (M <= 128) {
-    pl.swap_ab = 1;
-    pl.nx = swap_nx(M);
-    pl.w_tiles = N / 128;
-    pl.x_tiles = (M + pl.nx - 1) / pl.nx;
-    ctas_per_sm = pl.nx <= 32 ? 2 : 1;
-    tile_elems = static_cast<size_t>(128) * pl.nx;
-  } else {
-    // Large M: quantise A once into 128-row tiles, then stream both operands
-    // by TMA (inline quantisation would redo A for every 256-column tile).
-    pl.swap_ab = 0;
-    pl.prequant = 1;
-    pl.nx = 128;
-    pl.w_tiles = N / 256;
-    pl.x_tiles = (M + 127) / 128;
-    pl.aq_bytes = static_cast<size_t>(pl.x_tiles) * pl.kt * (16384 + 1024);
-    ctas_per_sm = 1;
-    tile_elems = static_cast<size_t>(128) * 256;
   }
+  // Swap-AB (17 <= M <= 128): weights on the MMA's 128-row side, up to 128
+  // tokens on N; K split over the SMs, reduced inside a cluster (at most 8).
+  pl.swap_ab = 1;
+  pl.nx = swap_nx(M);
+  pl.w_tiles = N / 128;
+  pl.x_tiles = (M + pl.nx - 1) / pl.nx;
+  const int ctas_per_sm = pl.nx <= 32 ? 2 : 1;
   const int tiles = pl.w_tiles * pl.x_tiles;
   int splits = (sms * ctas_per_sm) / (tiles > 0 ? tiles : 1);
   if (splits > pl.kt) splits = pl.kt;
+  if (splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   if (splits < 1) splits = 1;
-  // Swap-AB tiles always reduce inside a cluster (at most 8 splits); large-M
-  // tiles do when 8 splits are enough, else through the global workspace.
-  if ((pl.swap_ab || M <= 128) && splits > kMaxClusterSplits) splits = kMaxClusterSplits;
   pl.splits = splits;
-  pl.cluster_reduce = splits > 1 && splits <= kMaxClusterSplits;
-  if (pl.prequant && M > 128 && splits == 1) {
-    // At least one full wave of 128 x 256 tiles: one persistent CTA per SM
-    // walks them; a last wave of r tiles with 2r <= sms runs as 2r
-    // 128-column halves, so that it ends sooner.
-    pl.persistent = 1;
-    const int r = tiles % (sms > 0 ? sms : 1);
-    pl.half_tiles = (r > 0 && 2 * r <= sms) ? r : 0;
-  }
-  // workspace: [activation tiles][fp32 split-K partials][tile counters]
-  if (splits > 1 && !pl.cluster_reduce) {
-    pl.partial_bytes = static_cast<size_t>(tiles) * splits * tile_elems * sizeof(float);
-    pl.ws_bytes = pl.partial_bytes + ((static_cast<size_t>(tiles) * sizeof(unsigned int) + 255) & ~static_cast<size_t>(255));
-  }
-  pl.ws_bytes += pl.aq_bytes;
+  pl.cluster_reduce = splits > 1;
   return pl;
 }
 
@@ -954,15 +773,6 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
   a.Wq = static_cast<const uint8_t*>(Wq);
   a.Ws = static_cast<const uint8_t*>(Ws);
   a.C = static_cast<uint16_t*>(C);
-  uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if (pl.prequant) {
-    a.Aq = w8;               // 17 KB atoms: codes then scales
-    w8 += pl.aq_bytes;
-  }
-  if (pl.splits > 1 && !pl.cluster_reduce) {
-    a.partial = reinterpret_cast<float*>(w8);
-    a.counters = reinterpret_cast<unsigned int*>(w8 + pl.partial_bytes);
-  }
   a.M = M; a.N = N; a.K = K; a.KT = pl.kt; a.splits = pl.splits; a.w_tiles = pl.w_tiles;
   a.cluster_reduce = pl.cluster_reduce;
   a.wait_ns = wait_ns;
@@ -975,13 +785,14 @@ int launch_gemm(const GemmPlan& pl, const void* A, int M, int K, const void* Wq,
       default: return launch_cfg<kSwap, 128, 4>(a, grid, st);
     }
   }
-  if (pl.prequant) {
+  if (pl.persistent) {
+    // workspace: the activation tiles (17 KB atoms: codes then scales)
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int rc = launch_quant_activation_tiles(A, M, K, const_cast<uint8_t*>(a.Aq), st, sms);
+    uint8_t* aq = static_cast<uint8_t*>(ws);
+    const int rc = launch_quant_activation_tiles(A, M, K, aq, st, sms);
     if (rc != 0) return rc;
-    if (pl.persistent) return launch_large(pl, a.Aq, M, Wq, Ws, N, C, st, wait_ns, status, sms);
-    return launch_cfg<kPre, 128, 4>(a, grid, st);
+    return launch_large(pl, aq, M, Wq, Ws, N, C, st, wait_ns, status, sms);
   }
   return -4;   // every plan is one of the above
 }

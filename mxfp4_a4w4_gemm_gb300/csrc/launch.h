@@ -13,8 +13,8 @@ namespace a4w4 {
 struct GemmPlan {
   int swap_ab;      // 1: weights are the MMA's M side (small M)
   int decode;       // 1: the decode kernel (decode.cu): M <= 16, and some M <= 32 (plan_gemm)
-  int prequant;     // 1: activations quantised once into tiles first (large M)
-  int persistent;   // 1 (with prequant): the persistent large-M kernel (large.cu)
+  int prequant;     // 1: activations quantised once into tiles first (M > 128; M > 64 when N >= 4096)
+  int persistent;   // 1 (every prequant plan): the persistent large-M kernel (large.cu)
   int half_tiles;   // persistent: tiles of the last partial wave run as two 128-column halves
   size_t aq_bytes;  // workspace bytes of the quantised activation tiles (codes + scales)
   int nx;           // activation rows per CTA
@@ -24,8 +24,7 @@ struct GemmPlan {
   int ring;         // decode kernel: weight ring depth (K tiles in flight per CTA)
   int cluster_reduce;     // 1: the splits of a tile form a cluster and reduce over DSMEM
   int kt;           // 256-wide K tiles
-  size_t partial_bytes;   // fp32 split-K partial tiles
-  size_t ws_bytes;        // partial tiles + tile counters (0 without split-K)
+  size_t ws_bytes;        // workspace: the activation tiles (aq_bytes), or 0
 };
 
 GemmPlan plan_gemm(int M, int N, int K, int sms);

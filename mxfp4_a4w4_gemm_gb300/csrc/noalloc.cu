@@ -2,9 +2,7 @@
 //
 // a4w4_gemm() takes a caller-allocated workspace whenever its tile plan needs
 // one: for M > 64 (64 < M <= 128 when N >= 4096; every M > 128) the activations
-// are quantised once into MXFP4 tiles there, and for M > 128 a tile whose K
-// range is split over more CTAs than one thread-block cluster holds also keeps
-// its fp32 partial tiles and a tile counter there.  M <= 64 needs none.  Some
+// are quantised once into MXFP4 tiles there.  Smaller M needs none.  Some
 // callers cannot provide that memory: code running under a framework allocator
 // that owns all device memory, or a latency-critical path where cudaMalloc's
 // implicit device synchronisation is not acceptable.  This entry point runs the
@@ -17,12 +15,10 @@
 // that device (the call that looks its address up), and stays until the
 // process exits.  A plan that needs more than 16 MiB is refused with
 // A4W4_ERR_WORKSPACE; at K = 7168 that is M beyond about 4,400 rows (487 KB of
-// activation tiles per 128 rows), and shapes such as 200 x 1536 x 7168 whose
-// K split needs 18 MiB of partial tiles.  Every call shares the array, which
-// keeps whatever the previous call left there: the tile counters are cleared
-// on `stream` at the start of each call that uses them (the activation tiles
-// and partials are overwritten before they are read), and calls that can run
-// at the same time on one GPU (issued on different streams) race on it.
+// activation tiles per 128 rows).  Every call shares the array, which keeps
+// whatever the previous call left there (the activation tiles are overwritten
+// before they are read); calls that can run at the same time on one GPU
+// (issued on different streams) race on it.
 #include <atomic>
 #include <cstdint>
 
@@ -73,13 +69,6 @@ int a4w4_gemm_noalloc(const void* A_bf16, int M, int K, const void* Wq, const vo
   unsigned int* status = a4w4::device_status_ptr();
   if (status == nullptr) return A4W4_ERR_LAUNCH;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The split-K tile counters must start at zero; an earlier call (or one
-  // that timed out) may have left them otherwise.  They follow the activation
-  // tiles and the partial tiles in the scratch layout.
-  const size_t counters = plan.aq_bytes + plan.partial_bytes;
-  if (plan.ws_bytes > counters &&
-      cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counters, 0, plan.ws_bytes - counters, st) != cudaSuccess)
-    return A4W4_ERR_LAUNCH;
   return a4w4::launch_gemm(plan, A_bf16, M, K, Wq, Ws, N, C_bf16, plan.ws_bytes > 0 ? scratch : nullptr, st,
                            a4w4::wait_limit_ns(), status, 0, a4w4::ActDump{});
 }

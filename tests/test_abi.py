@@ -50,6 +50,7 @@ def test_size_functions():
     assert a4w4.a4w4_moe_max_blocks(1, 16, 896, 128) == 1 + 16
     # large M: activations quantised once into 128-row x 256-K tiles (16 KB codes + 1 KB scales each)
     assert a4w4.a4w4_gemm_workspace_bytes(2048, 8448, 7168) == 16 * 28 * (16384 + 1024)
+    assert a4w4.a4w4_gemm_workspace_bytes(200, 1536, 7168) == 2 * 28 * (16384 + 1024)   # no split-K partials
     # small M: split-K partials reduce inside a thread-block cluster, no workspace
     assert a4w4.a4w4_gemm_workspace_bytes(1, 1536, 7168) == 0
 
@@ -67,10 +68,11 @@ def test_kernel_routing_of_the_workload_shapes():
     assert name(1, 256, 16384 * 4) == "a4w4_decode_kernel<16,4>"    # a 3-deep ring would need > 16 splits
     assert name(37, 1536, 4224) == "a4w4_gemm_kernel<swap,64>"
     assert name(100, 1536, 4224) == "a4w4_gemm_kernel<swap,128>"     # N < 4096: swap-AB up to 128 tokens
-    assert name(128, 8448, 7168) == "a4w4_gemm_kernel<prequant,128>"
-    for M in (512, 2048):                                              # 128 x 256 tiles fill the SMs
+    for M in (128, 512, 2048):                                         # quantise once, persistent tile walk
         assert name(M, 8448, 7168) == "a4w4_large_kernel<prequant,persistent>"
-    assert name(513, 1536, 4224) == "a4w4_gemm_kernel<prequant,128>"  # 30 tiles: split-K instead
+    assert name(513, 1536, 4224) == "a4w4_large_kernel<prequant,persistent>"
+    assert name(65, 8448, 7168) == "a4w4_large_kernel<prequant,persistent>"   # N >= 4096: from 65 rows
+    assert name(128, 1536, 4224) == "a4w4_gemm_kernel<swap,128>"             # N < 4096: swap-AB to 128
     with pytest.raises(a4w4.A4W4Error) as e:
         name(1, 300, 256)
     assert e.value.code == a4w4.A4W4_ERR_ARG

@@ -175,11 +175,12 @@ def test_weight_prefetch_back_to_back(M, N, K):
 @pytest.mark.parametrize("M,N,K,family", [
     (1, 7168, 4224, "decode"),    # decode kernel: st.async split-K slices summed in rank order
     (32, 7168, 4224, "decode"),   # swap-AB: cluster push, owner sums in split order
-    (200, 1536, 7168, "large"),   # quantise-once tiles, global split-K partials, last CTA sums
-    (513, 1536, 4224, "stress"),  # quantise-once tiles, cluster pull reduction
+    (200, 1536, 7168, "large"),   # quantise-once tiles, persistent walk of column halves (no split-K)
+    (2048, 8448, 7168, "large"),  # persistent walk: 3 whole tiles per CTA, the last wave as halves
 ], ids=lambda v: str(v))
 def test_bitwise_deterministic_per_plan(M, N, K, family):
-    """Every split-K reduction sums in a fixed order: three runs give the same bits."""
+    """Every split-K reduction sums in a fixed order, and the persistent walk
+    has none: three runs give the same bits."""
     A, W = workloads.dense_problem(M, N, K, family)
     prep = Prepared(W)
     c1, ws = run_gemm(A, prep)

@@ -3,15 +3,14 @@
 It is for callers that cannot allocate device memory where they call the GEMM:
 code under a framework allocator that owns all device memory, or a path that
 cannot afford cudaMalloc's implicit synchronisation.  Its scratch (the
-activation tiles quantised once, and for some large-M plans fp32 split-K
-partial tiles and tile counters) is a fixed 16 MiB array in the library.
+activation tiles quantised once, for M > 64 with N >= 4096 and every M > 128)
+is a fixed 16 MiB array in the library.
 
 Each case calls it twice in a row through the C ABI and checks both outputs
 against the oracle with the tests' per-element tolerance, and bit for bit
 against a4w4_gemm with a caller workspace (same plan, same kernels, same
-reduction order).  The shapes cover a plan without scratch, plans whose
-scratch holds only activation tiles, and one with global split-K partials and
-counters.
+reduction order).  The shapes cover a plan without scratch and plans whose
+scratch holds the activation tiles, up to the largest workload shape.
 
 This file is collected last on purpose; it passes alone in a fresh process
 (the first call does the per-device set-up) and after the other tests."""
@@ -47,8 +46,8 @@ def prepared(W_bits):
 
 CASES = [
     (8, 1536, 7168, "decode"),      # decode kernel, cluster split-K: no scratch
-    (200, 512, 4224, "large"),      # activation tiles + global split-K partials and tile counters
-    (128, 8448, 7168, "large"),     # activation tiles, split-K inside clusters
+    (200, 512, 4224, "large"),      # activation tiles, 4 tiles run as 8 column halves
+    (128, 8448, 7168, "large"),     # activation tiles, one row tile (33 tiles as 66 halves)
     (513, 1536, 4224, "stress"),    # activation tiles, ragged M, scale-edge blocks
     (1024, 5120, 1536, "large"),    # activation tiles, no split-K
     (2048, 8448, 7168, "large"),    # the largest workload shape (7.4 MiB of tiles)
@@ -81,9 +80,9 @@ def test_noalloc_matches_oracle_and_workspace_gemm_twice(M, N, K, family):
 
 
 def test_noalloc_refuses_plans_beyond_its_scratch():
-    # 200 x 1536 x 7168 splits K 12 ways over 12 tiles of 128x256 fp32
-    # partials: 18 MiB of scratch, more than 16 MiB.
-    M, N, K = 200, 1536, 7168
+    # 4608 rows at K = 7168: 36 activation tiles x 28 K tiles x 17 KB =
+    # 17.5 MB of scratch, more than 16 MiB.
+    M, N, K = 4608, 256, 7168
     assert a4w4.a4w4_gemm_workspace_bytes(M, N, K) > SCRATCH_BYTES
     Wq, Ws = prepared(workloads.weight_bits(N, K))
     A = dev_bits(workloads.activation_bits(M, K))
