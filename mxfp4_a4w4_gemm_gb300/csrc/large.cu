@@ -19,10 +19,9 @@
 //              K = 64) per step; before a unit's first MMA it waits until the
 //              epilogue has read the previous unit's accumulator;
 //   warps 2-5  epilogue (one per TMEM lane quadrant, a thread per row):
-//              TMEM -> BF16 in 64-column chunks, turned around in a small
-//              per-warp buffer so that each store writes whole 128-byte row
-//              segments; the accumulator is handed back as soon as its last
-//              columns are in registers.
+//              the accumulator row -> packed BF16 registers, TMEM handed
+//              back, then 64-column chunks turned around in a small per-warp
+//              buffer so that each store writes whole 128-byte row segments.
 #include "device.cuh"
 #include "launch.h"
 
@@ -229,31 +228,40 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
       const int row0 = x_tile * 128 + q * 32;       // this warp's 32 rows
       const int cols = half < 0 ? 256 : 128;
       const int n0 = w_tile * 256 + (half > 0 ? 128 : 0);
-#pragma unroll 1
-      for (int c0 = 0; c0 < cols; c0 += 64) {
-        float v[64];
-        tmem_ld64(tq + c0, v);
-        if (c0 + 64 == cols) {
-          // the accumulator's last columns are in registers: the next unit's
-          // MMAs may overwrite it
-          tc_fence_before();
-          mbar_arrive(acc_empty);
-        }
-        // row lane -> buffer row; then 8 lanes per row, 4 rows per store
-        uint4* mine = reinterpret_cast<uint4*>(stg + lane * Cf::STG_PITCH);
+      // The whole accumulator row into registers first (packed BF16), so
+      // that TMEM goes back to the MMA warp before any store is issued.
+      uint32_t pk[128];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          mine[t] = make_uint4(bf16x2_bits(v[8 * t], v[8 * t + 1]), bf16x2_bits(v[8 * t + 2], v[8 * t + 3]),
-                               bf16x2_bits(v[8 * t + 4], v[8 * t + 5]), bf16x2_bits(v[8 * t + 6], v[8 * t + 7]));
-        __syncwarp();
+      for (int c0 = 0; c0 < 256; c0 += 64) {
+        if (c0 < cols) {
+          float v[64];
+          tmem_ld64(tq + c0, v);
 #pragma unroll
-        for (int r4 = 0; r4 < 8; ++r4) {
-          const int r = r4 * 4 + (lane >> 3), seg = lane & 7;
-          const uint4 val = *reinterpret_cast<const uint4*>(stg + r * Cf::STG_PITCH + seg * 16);
-          if (row0 + r < p.M)
-            *reinterpret_cast<uint4*>(p.C + static_cast<long long>(row0 + r) * p.N + n0 + c0 + seg * 8) = val;
+          for (int t = 0; t < 32; ++t) pk[c0 / 2 + t] = bf16x2_bits(v[2 * t], v[2 * t + 1]);
         }
-        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      // per 64-column chunk: row lane -> buffer row; then 8 lanes per row,
+      // 4 rows per store
+      uint4* mine = reinterpret_cast<uint4*>(stg + lane * Cf::STG_PITCH);
+#pragma unroll
+      for (int c0 = 0; c0 < 256; c0 += 64) {
+        if (c0 < cols) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            mine[t] = make_uint4(pk[c0 / 2 + 4 * t], pk[c0 / 2 + 4 * t + 1], pk[c0 / 2 + 4 * t + 2],
+                                 pk[c0 / 2 + 4 * t + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int r4 = 0; r4 < 8; ++r4) {
+            const int r = r4 * 4 + (lane >> 3), seg = lane & 7;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * Cf::STG_PITCH + seg * 16);
+            if (row0 + r < p.M)
+              *reinterpret_cast<uint4*>(p.C + static_cast<long long>(row0 + r) * p.N + n0 + c0 + seg * 8) = val;
+          }
+          __syncwarp();
+        }
       }
     }
   }
