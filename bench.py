@@ -492,10 +492,7 @@ class Moe2Sweep:
         return sum(2 * it["T"] * self.D for it in self.items)
 
     def kernel_name(self, i):
-        # the library's rule: few routed rows per expert -> the kernel with
-        # resident activation tiles, else one CTA per (block, column tile)
-        T = self.items[i]["T"]
-        return "a4w4_moe2_kernel" if T * self.topk <= 32 * self.E else "a4w4_gemm_kernel<moe2,128>"
+        return "a4w4_moe2_kernel"      # the persistent GEMM2 walk, every token count
 
     def launches_of(self, i):
         """GEMM2 and the per-token sum."""

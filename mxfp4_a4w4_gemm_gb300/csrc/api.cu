@@ -328,16 +328,11 @@ int a4w4_moe_gemm2(const void* A_q, const void* A_s, int T, int I, const int32_t
   if (status == nullptr) return A4W4_ERR_LAUNCH;
   const cudaStream_t st = as_stream(stream);
   float* partial = static_cast<float*>(ws);
-  // Blocks of few valid rows (up to 32 routed rows per expert on average):
-  // the kernel that keeps a block's activation tiles resident over many
-  // column tiles; otherwise one CTA per (block, column tile).
-  const bool few_rows = static_cast<long long>(T) * topk <= 32ll * E;
+  // The persistent walk (each block's activation tiles resident over its
+  // column tiles); the entry checks above keep I <= 1024, which it holds.
   const unsigned long long wait = g_wait_ns.load(std::memory_order_relaxed);
-  const int rc = few_rows ? a4w4::launch_moe_gemm2_resident(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks,
-                                                            max_blocks, topk, topk_weights, W2q, W2s, E, D, partial,
-                                                            st, wait, status, sms)
-                          : a4w4::launch_moe_gemm2(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, max_blocks,
-                                                   topk, topk_weights, W2q, W2s, E, D, partial, st, wait, status);
+  const int rc = a4w4::launch_moe_gemm2_persistent(A_q, A_s, T, I, sorted_rows, block_expert, num_blocks, max_blocks,
+                                                   topk, topk_weights, W2q, W2s, E, D, partial, st, wait, status, sms);
   if (rc != 0) return rc == -1 ? A4W4_ERR_ARG : rc;
   return a4w4::launch_moe_sum(partial, T, topk, D, Y_bf16, st, sms);
 }

@@ -31,22 +31,20 @@ namespace a4w4 {
 // the persistent kernel of large.cu); kMoe: inline-quantised gathered sorted
 // rows x an expert's weights with the SwiGLU / SiLU + requant epilogue;
 // kMoePre: kMoe gathering rows that were quantised once beforehand (plain
-// MXFP4 layout) instead of quantising them per tile; kMoe2: MoE GEMM2, GEMM1's
-// output tiles (sorted-slot operand layout) streamed by TMA against the
-// expert's down projection, top-k weighted fp32 rows out.
-enum Mode { kSwap = 0, kMoe = 1, kMoePre = 2, kMoe2 = 3 };
+// MXFP4 layout) instead of quantising them per tile.  (MoE GEMM2 runs in the
+// persistent kernel of moe2.cu.)
+enum Mode { kSwap = 0, kMoe = 1, kMoePre = 2 };
 
 // MoE GEMM1 epilogue activation (a4w4.h: A4W4_MOE_ACT_*)
 constexpr int kActSwiglu = 0, kActSilu = 1;
 
 struct GemmArgs {
   const uint16_t* A;  // dense: activations [M, K]; MoE: tokens X [T, D]
-  const uint8_t* Aq;  // kMoe2: activation tiles (weight layout), codes; kMoePre: MXFP4 rows
-  const uint8_t* As;  // kMoe2: activation tiles, scales; kMoePre: E8M0 rows
+  const uint8_t* Aq;  // kMoePre: tokens quantised once, MXFP4 codes [T, K/2]
+  const uint8_t* As;  // kMoePre: their E8M0 scales [T, K/32]
   const uint8_t* Wq;
   const uint8_t* Ws;
   uint16_t* C;        // [M, N] BF16
-  float* partial;        // kMoe2: [T*topk, D] fp32 weighted rows
   int M, N, K, KT, splits, w_tiles;
   int cluster_reduce;   // 1: the `splits` CTAs of a tile form a cluster and reduce over DSMEM
   int prefetch_w;       // 1: weights may be read before the previous grid on the stream completes
@@ -63,7 +61,6 @@ struct GemmArgs {
   int act;              // kActSwiglu or kActSilu
   int out_tiles;        // 1: GEMM1 output in sorted-slot operand tiles (KT_out K tiles per block)
   int KT_out;
-  const float* topk_w;  // GEMM2: routing weight of each routed row
   // test hook (ActDump): the CTAs of weight tile 0 also store the activation
   // tiles their producers build; nullptr in every product call
   uint8_t* dump_codes;
@@ -79,11 +76,10 @@ struct Cfg {
   static constexpr int NW = kSwapAB ? 128 : 256;                 // weight rows per CTA
   static constexpr int W_ATOMS = NW / 128;
   static constexpr int MMA_N = kSwapAB ? NX : NW;
-  static constexpr bool kTmaA = MODE == kMoe2;                  // activations arrive by TMA too
   static constexpr bool kMoeAny = MODE == kMoe || MODE == kMoePre;  // MoE GEMM1
-  static constexpr bool kRouted = kMoeAny || MODE == kMoe2;        // blocks of sorted routed rows
+  static constexpr bool kRouted = kMoeAny;                       // blocks of sorted routed rows
   static constexpr bool kGatherQ = MODE == kMoePre;              // producers copy pre-quantised rows
-  static constexpr int QWARPS = ((kSwapAB && NX <= 32) || kTmaA) ? 4 : 8;   // producer warps
+  static constexpr int QWARPS = (kSwapAB && NX <= 32) ? 4 : 8;   // producer warps
   // epilogue warps (the first of the producer warps): MoE's SwiGLU + requant
   // epilogue splits each TMEM lane quadrant's columns over two warps
   static constexpr int EPI_WARPS = kMoeAny ? 8 : 4;
@@ -175,31 +171,21 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   // Activation rows that do not exist (beyond M, or padding of a routed
   // block) are never written by the producers: their codes and scales are
   // zeroed here once for every stage.
-  if (!Cf::kTmaA) {
-    for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
-      reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int i = threadIdx.x; i < STAGES * Cf::X_CODE_BYTES / 16; i += Cf::THREADS)
+    reinterpret_cast<uint4*>(smem + Cf::OFF_X)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < STAGES * Cf::X_SF_BYTES / 16; i += Cf::THREADS)
+    reinterpret_cast<uint4*>(smem + Cf::OFF_XSF)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   __syncthreads();                                 // barriers initialised
   // Start streaming weights before TMEM allocation: the first ring pass needs
   // no empty-slot wait (fresh barriers).
   const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
   const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
-  // Swap-AB and MoE GEMM1 stream every weight byte once.  MoE GEMM2 reads
-  // each block's activation tiles once per output-column tile (evict-last)
-  // and the expert's weights about once (evict-first).
+  // Swap-AB and MoE GEMM1 stream every weight byte once.
   const uint64_t pol = policy_evict_first();
-  const uint64_t pol_a = Cf::kTmaA ? policy_evict_last() : pol;
   auto issue_stage = [&](int i) {
     const int s = i % STAGES;
-    mbar_arrive_expect_tx(full_w(s), (Cf::W_ATOMS + (Cf::kTmaA ? 1 : 0)) * (16384 + 1024));
-    if (Cf::kTmaA) {
-      const long long atom = static_cast<long long>(x_tile) * p.KT + (kt0 + i);
-      bulk_g2s(base + Cf::OFF_X + s * Cf::X_CODE_BYTES, p.Aq + atom * 16384, 16384, full_w(s), pol_a);
-      bulk_g2s(base + Cf::OFF_XSF + s * Cf::X_SF_BYTES, p.As + atom * 1024, 1024, full_w(s), pol_a);
-    }
+    mbar_arrive_expect_tx(full_w(s), Cf::W_ATOMS * (16384 + 1024));
     // the W_ATOMS atoms of this K tile are adjacent (weight_atom): one copy
     // of codes, one of scales
     const long long watom = weight_atom(w_tile * Cf::W_ATOMS, kt0 + i, p.KT);
@@ -209,10 +195,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
   int issued = 0;
   if (warp == 0 && lane == 0) {
     // Weights are read before the grid dependency resolves only on request
-    // (the previous kernel on the stream must not write them), and never when
-    // a stage also carries activation tiles: those come from the kernel just
-    // before this one.
-    if (!p.prefetch_w || Cf::kTmaA) griddep_wait();
+    // (the previous kernel on the stream must not write them).
+    if (!p.prefetch_w) griddep_wait();
     issued = nk < STAGES ? nk : STAGES;
     for (int i = 0; i < issued; ++i) issue_stage(i);
   }
@@ -270,7 +254,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       uint32_t ph = 0;
       for (int i = 0; i < nk; ++i) {
         if (!mbar_wait(full_w(s), ph, abort_flag, p.wait_ns, p.status) ||
-            (!Cf::kTmaA && !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status))) {
+            !mbar_wait(full_x(s), ph, abort_flag, p.wait_ns, p.status)) {
           ok = false;
           break;
         }
@@ -391,7 +375,7 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
       fence_proxy_async_smem();
       mbar_arrive(full_x(s));
     };
-    const int nq = Cf::kTmaA ? 0 : nk;
+    const int nq = nk;
     if constexpr (Cf::kGatherQ) {
       // Rows were quantised once beforehand (codes [T, K/2], scales [T, K/32]):
       // copy this thread's 16-byte code chunks and scale bytes of a stage into
@@ -530,31 +514,6 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
               for (int i = et; i < n4; i += 128)
                 st_shared_cluster_v4(cluster_map_shared(slot + static_cast<uint32_t>(i * 16), static_cast<uint32_t>(o)), src[i]);
             }
-          }
-        } else if (MODE == kMoe2) {
-          // MoE GEMM2: each valid sorted slot's fp32 row (256 output columns)
-          // times its routing weight, staged in the drained ring (pitch 1040
-          // bytes) and written to row `entry` of the [T*topk, D] partial
-          // buffer with one 1 KB bulk store; padding slots write nothing.
-          const int entry = p.sorted_rows[x_tile * 128 + lrow];
-          const bool valid = entry >= 0 && entry < p.routed_rows;
-          const float wgt = valid ? __ldg(p.topk_w + entry) : 0.f;
-          constexpr int kRowPitch = 1040;
-          float* my = reinterpret_cast<float*>(smem + lrow * kRowPitch);
-#pragma unroll 1
-          for (int c0 = 0; c0 < 256; c0 += 64) {
-            float v[64];
-            tmem_ld64(tq + c0, v);
-            float4* d = reinterpret_cast<float4*>(my + c0);
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              d[j] = make_float4(wgt * v[4 * j], wgt * v[4 * j + 1], wgt * v[4 * j + 2], wgt * v[4 * j + 3]);
-          }
-          fence_proxy_async_smem();
-          if (valid) {
-            bulk_s2g(p.partial + static_cast<long long>(entry) * p.N + w_tile * 256,
-                     base + static_cast<uint32_t>(lrow * kRowPitch), 1024);
-            bulk_commit_wait_read();
           }
         } else {  // kMoe, kMoePre: activation + MXFP4 requant of the CTA's output columns
           // SwiGLU: 128 output columns per CTA (accumulator columns 0..127
@@ -838,34 +797,6 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
     return launch_cfg<kMoePre, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
   }
   return launch_cfg<kMoe, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
-}
-
-int launch_moe_gemm2(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
-                     const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
-                     const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
-                     cudaStream_t st, unsigned long long wait_ns, unsigned int* status) {
-  GemmArgs a{};
-  a.status = status;
-  a.Aq = static_cast<const uint8_t*>(Aq);
-  a.As = static_cast<const uint8_t*>(As);
-  a.Wq = static_cast<const uint8_t*>(W2q);
-  a.Ws = static_cast<const uint8_t*>(W2s);
-  a.M = T; a.N = D; a.K = I; a.KT = (I + 255) / 256; a.splits = 1; a.w_tiles = D / 256;
-  a.wait_ns = wait_ns;
-  a.sorted_rows = sorted_rows;
-  a.block_expert = block_expert;
-  a.num_blocks = num_blocks;
-  a.topk = topk;
-  a.routed_rows = T * topk;
-  a.I = I;
-  a.E = E;
-  a.topk_w = topk_w;
-  a.partial = partial;
-  const long long kp = static_cast<long long>(a.KT) * 256;
-  a.expert_code_bytes = static_cast<long long>(D) * kp / 2;
-  a.expert_sf_bytes = static_cast<long long>(D) * kp / 32;
-  if (max_blocks <= 0) return 0;
-  return launch_cfg<kMoe2, 128, 4>(a, dim3(a.w_tiles, max_blocks, 1), st);
 }
 
 }  // namespace a4w4

@@ -114,19 +114,13 @@ int launch_moe_gemm1(const void* X, int T, int D, const int32_t* sorted_rows, co
                      int E, int I, int act, int out_tiles, void* out_q, void* out_s, void* xq_ws, cudaStream_t st,
                      unsigned long long wait_ns, unsigned int* status, int sms, ActDump dump);
 // MoE GEMM2: GEMM1's sorted-slot tiles x W2[e] ([D, I] dense layout per
-// expert) -> top-k weighted fp32 rows partial[T*topk, D].  Two kernels:
-// one CTA per (block, 256-column tile) staging each valid row for one bulk
-// store (gemm.cu), or (moe2.cu, I <= 1024) one CTA per (block, run of
-// column tiles) with the block's activation tiles resident, storing valid
-// rows from registers -- the faster one when blocks hold few valid rows.
-int launch_moe_gemm2(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
-                     const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
-                     const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
-                     cudaStream_t st, unsigned long long wait_ns, unsigned int* status);
-int launch_moe_gemm2_resident(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
-                              const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
-                              const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
-                              cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int sms);
+// expert, I <= 1024) -> top-k weighted fp32 rows partial[T*topk, D]: one
+// persistent CTA per SM walking a contiguous run of (block, 256-column tile)
+// units with each block's activation tiles resident (moe2.cu).
+int launch_moe_gemm2_persistent(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
+                                const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
+                                const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
+                                cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int sms);
 // Y[t, :] (BF16) = sum over k = 0..topk-1, in that order, of partial[t*topk + k, :].
 int launch_moe_sum(const float* partial, int T, int topk, int D, void* Y, cudaStream_t st, int sms);
 int launch_moe_sort(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_rows,

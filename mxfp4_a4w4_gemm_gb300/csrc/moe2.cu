@@ -4,23 +4,26 @@
 // "[HIP] [CK] [FlyDSL] [Kernel] Extend MXFP4 GEMM1 replacement to A4W4",
 // Summary (stage-2 paths that consume stage 1's layout) and GEMM2 scope.
 //
-// One CTA per (sorted block of 128 slots, run of output-column tiles): the
-// block's activation tiles (K = I, a few 256-wide atoms) are copied into
-// shared memory once; the expert's W2 tiles of the run (256 output rows x
-// 256 K, one 32 KB + 2 KB copy each) stream through a ring.  A block routed
-// to one expert usually holds few valid rows, so a CTA walks many tiles with
-// its operand rows resident instead of reloading them per tile.
-//   warp 0      copies the activation tiles, then the weight ring;
-//   warp 1      allocates TMEM, copies the activation scales to TMEM once and
-//               each stage's weight scales, issues four
-//               tcgen05.mma.kind::mxf4.block_scale (M = 128, N = 256, K = 64)
-//               per K tile, commits the tile's accumulator to the epilogue;
-//   warps 2-5   per tile: wait for the accumulator, then per 64 columns
-//               tcgen05.ld, scale each valid row by its routing weight and
-//               store it from registers (row `routed row` of
-//               the [T*topk, D] fp32 partial buffer); then hand the
-//               accumulator back (the next tile's weights keep streaming
-//               meanwhile; only its MMAs wait).
+// Persistent: one CTA per SM takes a contiguous run of work units (sorted
+// block b, 256-column output tile w), numbered block by block, so that a
+// block's activation tiles (K = I, at most four 17 KB atoms) are copied into
+// shared memory once and stay while the CTA walks that block's tiles; the
+// expert's W2 tiles (256 output rows x 256 K, one 32 KB + 2 KB copy each)
+// stream through a ring that runs on across units and blocks.
+//   warp 0      copies a block's activation tiles when the block changes
+//               (after the previous block's MMAs have finished), and the
+//               weight ring;
+//   warp 1      allocates TMEM, copies the activation scales to TMEM per
+//               block and each stage's weight scales, and issues per K tile
+//               eight tcgen05.mma.kind::mxf4.block_scale (M = 128, N = 128,
+//               K = 64): the tile's two column halves go to two of three
+//               128-column accumulator slots, so the next unit's MMAs start as
+//               soon as the epilogue has read one slot;
+//   warps 2-5   per slot: tcgen05.ld of the 128 columns into registers, the
+//               slot handed back, each valid row scaled by its routing weight
+//               and written, through a small per-warp turnaround buffer, as
+//               whole 128-byte row segments of row `routed row` of the
+//               [T*topk, D] fp32 partial buffer.
 #include <atomic>
 
 #include "device.cuh"
@@ -39,7 +42,7 @@ struct Moe2Args {
   const int32_t* num_blocks;
   const float* topk_w;
   float* partial;            // [T*topk, D] fp32
-  int routed_rows, D, KT, E, tiles_per_cta;
+  int routed_rows, D, KT, E;
   unsigned long long wait_ns;
   unsigned int* status;
 };
@@ -47,16 +50,20 @@ struct Moe2Args {
 constexpr int kM2Stages = 4;
 constexpr int kM2MaxKT = 4;                              // I <= 1024
 constexpr int kM2Threads = 192;
+constexpr int kM2StgPitch = 144;                         // turnaround row: 32 fp32 + 16 bytes
 constexpr int kM2OffA = 0;                               // activation codes, KT x 16 KB
 constexpr int kM2OffAsf = kM2OffA + kM2MaxKT * 16384;    // activation scales, KT x 1 KB
 constexpr int kM2OffW = kM2OffAsf + kM2MaxKT * 1024;     // weight ring, 32 KB per stage
 constexpr int kM2OffWsf = kM2OffW + kM2Stages * 32768;   // weight scales, 2 KB per stage
-constexpr int kM2OffBar = kM2OffWsf + kM2Stages * 2048;
-constexpr int kM2OffMisc = kM2OffBar + (2 * kM2Stages + 3) * 8;
+constexpr int kM2OffStg = kM2OffWsf + kM2Stages * 2048;  // 4 warps x 32 rows
+constexpr int kM2OffBar = kM2OffStg + 4 * 32 * kM2StgPitch;
+constexpr int kM2NBar = 2 * kM2Stages + 2 + 3 + 3 + 1;   // ring; A full/empty; slot full x3, empty x3; drain
+constexpr int kM2OffMisc = kM2OffBar + kM2NBar * 8;
 constexpr int kM2Smem = kM2OffMisc + 32 + 1024;
-constexpr int kM2TmemCols = 512;                         // 256 accumulator + scale columns
-constexpr int kM2SfaCol = 256;                           // activation scales: 8 per K tile
+constexpr int kM2TmemCols = 512;
+constexpr int kM2SfaCol = 384;                           // after three 128-column accumulator slots
 constexpr int kM2SfbCol = kM2SfaCol + 8 * kM2MaxKT;      // weight scales: 16 per stage
+static_assert(kM2OffW % 1024 == 0, "swizzled tiles start 1024-aligned");
 static_assert(kM2SfbCol + 16 * kM2Stages <= kM2TmemCols, "TMEM budget");
 static_assert(kM2Smem <= 232448, "shared memory");
 
@@ -66,26 +73,17 @@ __global__ void __launch_bounds__(kM2Threads, 1) a4w4_moe2_kernel(const Moe2Args
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.y;
-
-  griddep_wait();                                  // GEMM1 and the sort have completed
-  griddep_launch_dependents();
-  if (blk >= *p.num_blocks) return;
-  const int expert = p.block_expert[blk];
-  if (expert < 0 || expert >= p.E) return;
-  const int wt_total = p.D / 256;
-  const int wt0 = blockIdx.x * p.tiles_per_cta;
-  const int wt1 = min(wt_total, wt0 + p.tiles_per_cta);
-  if (wt0 >= wt1) return;
-  const int ntile = wt1 - wt0, KT = p.KT, nstage = ntile * KT;
   const unsigned long long drain_ns = p.wait_ns > 100000000ull ? p.wait_ns : 100000000ull;
+  const int KT = p.KT, WT = p.D / 256;
 
   const uint32_t bar0 = base + kM2OffBar;
   auto w_full = [&](int s) { return bar0 + 8u * s; };
   auto w_empty = [&](int s) { return bar0 + 8u * (kM2Stages + s); };
-  const uint32_t a_full = bar0 + 8u * (2 * kM2Stages);
-  const uint32_t acc_full = a_full + 8u;
-  const uint32_t acc_empty = acc_full + 8u;
+  const uint32_t a_full = bar0 + 8u * (2 * kM2Stages);    // a block's activation tiles landed
+  const uint32_t a_empty = a_full + 8u;                   // the block's MMAs have finished
+  auto slot_full = [&](int k) { return a_empty + 8u * (1 + k); };
+  auto slot_empty = [&](int k) { return a_empty + 8u * (4 + k); };
+  const uint32_t drain = a_empty + 8u * 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kM2OffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kM2OffMisc + 8);
   volatile int* never = reinterpret_cast<volatile int*>(smem + kM2OffMisc + 16);
@@ -96,123 +94,197 @@ __global__ void __launch_bounds__(kM2Threads, 1) a4w4_moe2_kernel(const Moe2Args
       mbar_init(w_empty(s), 1);
     }
     mbar_init(a_full, 1);
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(a_empty, 1);
+    for (int k = 0; k < 3; ++k) {
+      mbar_init(slot_full(k), 1);
+      mbar_init(slot_empty(k), 128);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kM2TmemCols);
+    tc_fence_before();
+  }
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();                                  // GEMM1 and the sort have completed
+  griddep_launch_dependents();
 
-  const uint8_t* wq_e = p.Wq + static_cast<long long>(expert) * p.expert_code_bytes;
-  const uint8_t* ws_e = p.Ws + static_cast<long long>(expert) * p.expert_sf_bytes;
-  uint32_t tmem = 0;
+  // This CTA's units [u0, u1) of nb x WT, in order; a unit whose block has
+  // no valid expert is skipped by every role alike.
+  const long long units = static_cast<long long>(*p.num_blocks) * WT;
+  const int u0 = static_cast<int>(units * blockIdx.x / gridDim.x);
+  const int u1 = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
+  auto expert_of = [&](int b) {
+    const int e = p.block_expert[b];
+    return (e >= 0 && e < p.E) ? e : -1;
+  };
 
   if (warp == 0) {
     // ---------------- copies ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();   // each W2 tile is read by this CTA only
+      const uint64_t pol_w = policy_evict_first();   // each W2 tile is read by one CTA (about once)
       const uint64_t pol_a = policy_evict_first();
-      mbar_arrive_expect_tx(a_full, KT * (16384 + 1024));
-      bulk_g2s(base + kM2OffA, p.Aq + static_cast<long long>(blk) * KT * 16384, KT * 16384, a_full, pol_a);
-      bulk_g2s(base + kM2OffAsf, p.As + static_cast<long long>(blk) * KT * 1024, KT * 1024, a_full, pol_a);
-      int i = 0;
-      for (; i < nstage; ++i) {
-        const int s = i % kM2Stages;
-        if (i >= kM2Stages && !mbar_wait(w_empty(s), ((i / kM2Stages) & 1) ^ 1u, abort_flag, p.wait_ns, p.status))
-          break;
-        const int wt = wt0 + i / KT, kt = i % KT;
-        const long long atom = weight_atom(2 * wt, kt, KT);   // the tile's two 128-row atoms, adjacent
-        mbar_arrive_expect_tx(w_full(s), 32768 + 2048);
-        bulk_g2s(base + kM2OffW + s * 32768, wq_e + atom * 16384, 32768, w_full(s), pol_w);
-        bulk_g2s(base + kM2OffWsf + s * 2048, ws_e + atom * 1024, 2048, w_full(s), pol_w);
+      int cur_b = -1, loads = 0, g = 0;
+      bool ok = true;
+      for (int u = u0; u < u1 && ok; ++u) {
+        const int b = u / WT, wt = u % WT;
+        const int e = expert_of(b);
+        if (e < 0) continue;
+        if (b != cur_b) {
+          // the previous block's MMAs have finished reading its tiles
+          if (loads > 0 && !mbar_wait(a_empty, static_cast<uint32_t>((loads - 1) & 1), abort_flag, p.wait_ns, p.status))
+            break;
+          mbar_arrive_expect_tx(a_full, KT * (16384 + 1024));
+          bulk_g2s(base + kM2OffA, p.Aq + static_cast<long long>(b) * KT * 16384, KT * 16384, a_full, pol_a);
+          bulk_g2s(base + kM2OffAsf, p.As + static_cast<long long>(b) * KT * 1024, KT * 1024, a_full, pol_a);
+          ++loads;
+          cur_b = b;
+        }
+        const uint8_t* wq_e = p.Wq + static_cast<long long>(e) * p.expert_code_bytes;
+        const uint8_t* ws_e = p.Ws + static_cast<long long>(e) * p.expert_sf_bytes;
+        for (int kt = 0; kt < KT; ++kt) {
+          const int s = g % kM2Stages;
+          if (!mbar_wait(w_empty(s), ((g / kM2Stages) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          const long long atom = weight_atom(2 * wt, kt, KT);   // the tile's two 128-row atoms, adjacent
+          mbar_arrive_expect_tx(w_full(s), 32768 + 2048);
+          bulk_g2s(base + kM2OffW + s * 32768, wq_e + atom * 16384, 32768, w_full(s), pol_w);
+          bulk_g2s(base + kM2OffWsf + s * 2048, ws_e + atom * 1024, 2048, w_full(s), pol_w);
+          ++g;
+        }
       }
       // every copy issued lands before the shared memory is released
-      mbar_wait(a_full, 0, never, drain_ns, p.status);
-      for (int j = (i > kM2Stages ? i - kM2Stages : 0); j < i; ++j)
+      if (loads > 0) mbar_wait(a_full, static_cast<uint32_t>((loads - 1) & 1), never, drain_ns, p.status);
+      for (int j = (g > kM2Stages ? g - kM2Stages : 0); j < g; ++j)
         mbar_wait(w_full(j % kM2Stages), (j / kM2Stages) & 1u, never, drain_ns, p.status);
     }
   } else if (warp == 1) {
-    // ---------------- TMEM + MMA ----------------
-    tmem_alloc(smem_u32(tmem_slot), kM2TmemCols);
-    tc_fence_before();
-    __syncwarp();
-    tc_fence_after();
-    tmem = *tmem_slot;
-    named_bar_arrive(2, 32 + 128);                 // publish the TMEM address to the epilogue
+    // ---------------- scale copies + MMA ----------------
     if (lane == 0) {
-      int issued_tiles = 0;
-      if (mbar_wait(a_full, 0, abort_flag, p.wait_ns, p.status)) {
-        tc_fence_after();
-        const uint64_t asfd = sdesc_sf(base + kM2OffAsf), wsfd = sdesc_sf(base + kM2OffWsf);
-        for (int kt = 0; kt < KT; ++kt)
-          for (int ka = 0; ka < 2; ++ka)
-            tmem_copy_sf_desc(tmem + kM2SfaCol + kt * 8 + ka * 4, asfd + ((kt * 1024 + ka * 512) >> 4));
-        const uint64_t adesc0 = sdesc_sw128(base + kM2OffA), wdesc0 = sdesc_sw128(base + kM2OffW);
-        const uint32_t idesc0 = idesc_mxf4(256, 0, 0), idesc2 = idesc_mxf4(256, 2, 2);
-        bool ok = true;
-        for (int j = 0; j < ntile && ok; ++j) {
-          // the epilogue has read the previous tile's accumulator
-          if (j > 0 && !mbar_wait(acc_empty, (j - 1) & 1u, abort_flag, p.wait_ns, p.status)) break;
+      const uint64_t asfd = sdesc_sf(base + kM2OffAsf), wsfd = sdesc_sf(base + kM2OffWsf);
+      const uint64_t adesc0 = sdesc_sw128(base + kM2OffA), wdesc0 = sdesc_sw128(base + kM2OffW);
+      const uint32_t idesc0 = idesc_mxf4(128, 0, 0), idesc2 = idesc_mxf4(128, 2, 2);
+      int cur_b = -1, loads = 0, g = 0, pos = 0;
+      bool ok = true;
+      for (int u = u0; u < u1 && ok; ++u) {
+        const int b = u / WT;
+        if (expert_of(b) < 0) continue;
+        if (b != cur_b) {
+          if (cur_b >= 0) mma_commit(a_empty);   // the previous block's tiles are free once its MMAs finish
+          if (!mbar_wait(a_full, static_cast<uint32_t>(loads & 1), abort_flag, p.wait_ns, p.status)) break;
           tc_fence_after();
-          for (int kt = 0; kt < KT; ++kt) {
-            const int i = j * KT + kt, s = i % kM2Stages;
-            if (!mbar_wait(w_full(s), (i / kM2Stages) & 1u, abort_flag, p.wait_ns, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sfb = tmem + kM2SfbCol + s * 16;
+          for (int kt = 0; kt < KT; ++kt)
             for (int ka = 0; ka < 2; ++ka)
-              for (int a = 0; a < 2; ++a)
-                tmem_copy_sf_desc(sfb + ka * 8 + a * 4, wsfd + ((s * 2048 + a * 1024 + ka * 512) >> 4));
-            const uint64_t ad = adesc0 + ((kt * 16384) >> 4), wd = wdesc0 + ((s * 32768) >> 4);
+              tmem_copy_sf_desc(tmem + kM2SfaCol + kt * 8 + ka * 4, asfd + ((kt * 1024 + ka * 512) >> 4));
+          ++loads;
+          cur_b = b;
+        }
+        // the tile's two column halves go to accumulator slots pos % 3 and
+        // (pos + 1) % 3; wait until the epilogue has read their last use
+        int slot[2];
+        for (int h = 0; h < 2; ++h) {
+          const int q = pos + h, k = q % 3, use = q / 3;
+          slot[h] = k;
+          if (use > 0 && !mbar_wait(slot_empty(k), static_cast<uint32_t>((use - 1) & 1), abort_flag, p.wait_ns, p.status))
+            ok = false;
+        }
+        if (!ok) break;
+        tc_fence_after();
+        for (int kt = 0; kt < KT; ++kt) {
+          const int s = g % kM2Stages;
+          if (!mbar_wait(w_full(s), (g / kM2Stages) & 1u, abort_flag, p.wait_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfb = tmem + kM2SfbCol + s * 16;
+          for (int ka = 0; ka < 2; ++ka)
+            for (int a = 0; a < 2; ++a)
+              tmem_copy_sf_desc(sfb + ka * 8 + a * 4, wsfd + ((s * 2048 + a * 1024 + ka * 512) >> 4));
+          const uint64_t ad = adesc0 + ((kt * 16384) >> 4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t wd = wdesc0 + ((s * 32768 + h * 16384) >> 4);   // rows 128h .. 128h+127 of the tile
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const int ka = ks >> 1;
-              mma_mxf4(tmem, ad + ks * 2, wd + ks * 2, (ks & 1) ? idesc2 : idesc0, tmem + kM2SfaCol + kt * 8 + ka * 4,
-                       sfb + ka * 8, (kt > 0 || ks > 0) ? 1u : 0u);
+              mma_mxf4(tmem + slot[h] * 128, ad + ks * 2, wd + ks * 2, (ks & 1) ? idesc2 : idesc0,
+                       tmem + kM2SfaCol + kt * 8 + ka * 4, sfb + ka * 8 + h * 4, (kt > 0 || ks > 0) ? 1u : 0u);
             }
-            mma_commit(w_empty(s));
           }
-          if (!ok) break;
-          mma_commit(acc_full);
-          issued_tiles = j + 1;
+          mma_commit(w_empty(s));
+          ++g;
         }
+        if (!ok) break;
+        mma_commit(slot_full(slot[0]));
+        mma_commit(slot_full(slot[1]));
+        pos += 2;
       }
-      // TMEM is not released while MMAs may run: wait for the last commit
-      if (issued_tiles > 0) mbar_wait(acc_full, (issued_tiles - 1) & 1u, never, drain_ns, p.status);
+      // TMEM is not released while MMAs may run
+      mma_commit(drain);
+      mbar_wait(drain, 0, never, drain_ns, p.status);
     }
   } else {
     // ---------------- epilogue (warps 2-5, one TMEM lane quadrant each) ----------------
-    named_bar_sync(2, 32 + 128);
-    tc_fence_after();
-    tmem = *tmem_slot;
     const int q = warp & 3, lrow = q * 32 + lane;
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int entry = p.sorted_rows[blk * 128 + lrow];
-    const bool valid = entry >= 0 && entry < p.routed_rows;
-    const float wgt = valid ? __ldg(p.topk_w + entry) : 0.f;
-    float* out_row = p.partial + static_cast<long long>(valid ? entry : 0) * p.D;
-    for (int j = 0; j < ntile; ++j) {
-      // every thread waits itself (a bounded wait; no barrier that one
-      // thread's early exit could leave waiting)
-      if (!mbar_wait(acc_full, j & 1u, abort_flag, p.wait_ns, p.status)) break;
-      tc_fence_after();
-      const int wt = wt0 + j;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 64) {
-        float v[64];
-        tmem_ld64(tq + c0, v);
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(out_row + wt * 256 + c0);
+    uint8_t* stg = smem + kM2OffStg + (warp - 2) * 32 * kM2StgPitch;
+    int cur_b = -1, entry = 0, pos = 0;
+    bool valid = false, ok = true;
+    float wgt = 0.f;
+    for (int u = u0; u < u1 && ok; ++u) {
+      const int b = u / WT, wt = u % WT;
+      if (expert_of(b) < 0) continue;
+      if (b != cur_b) {
+        entry = p.sorted_rows[b * 128 + lrow];
+        valid = entry >= 0 && entry < p.routed_rows;
+        wgt = valid ? __ldg(p.topk_w + entry) : 0.f;
+        cur_b = b;
+      }
+      for (int h = 0; h < 2; ++h) {
+        const int qq = pos + h, k = qq % 3, use = qq / 3;
+        if (!mbar_wait(slot_full(k), static_cast<uint32_t>(use & 1), abort_flag, p.wait_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        tc_fence_after();
+        float v[128];
+        tmem_ld64(tq + k * 128, v);
+        tmem_ld64(tq + k * 128 + 64, v + 64);
+        tc_fence_before();
+        mbar_arrive(slot_empty(k));              // the slot may take the next unit's MMAs
+        const int n0 = wt * 256 + h * 128;
+        uint4* mine = reinterpret_cast<uint4*>(stg + lane * kM2StgPitch);
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            __stcs(dst + u, make_float4(wgt * v[4 * u], wgt * v[4 * u + 1], wgt * v[4 * u + 2], wgt * v[4 * u + 3]));
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const float* x = v + c * 32 + 4 * t;
+            mine[t] = make_uint4(__float_as_uint(wgt * x[0]), __float_as_uint(wgt * x[1]), __float_as_uint(wgt * x[2]),
+                                 __float_as_uint(wgt * x[3]));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int r4 = 0; r4 < 8; ++r4) {
+            const int r = r4 * 4 + (lane >> 3), seg = lane & 7;
+            const int er = __shfl_sync(0xffffffffu, entry, r);
+            const int vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, r);
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + r * kM2StgPitch + seg * 16);
+            if (vr)
+              __stcs(reinterpret_cast<uint4*>(p.partial + static_cast<long long>(er) * p.D + n0 + c * 32 + seg * 4), val);
+          }
+          __syncwarp();
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
+      pos += 2;
     }
   }
 
@@ -225,7 +297,7 @@ __global__ void __launch_bounds__(kM2Threads, 1) a4w4_moe2_kernel(const Moe2Args
   }
 }
 
-int launch_moe_gemm2_resident(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
+int launch_moe_gemm2_persistent(const void* Aq, const void* As, int T, int I, const int32_t* sorted_rows,
                      const int32_t* block_expert, const int32_t* num_blocks, int max_blocks, int topk,
                      const float* topk_w, const void* W2q, const void* W2s, int E, int D, float* partial,
                      cudaStream_t st, unsigned long long wait_ns, unsigned int* status, int sms) {
@@ -250,15 +322,10 @@ int launch_moe_gemm2_resident(const void* Aq, const void* As, int T, int I, cons
   a.E = E;
   a.wait_ns = wait_ns;
   a.status = status;
-  // Output-column tiles per CTA: all of them once the blocks alone give two
-  // CTAs per SM; fewer (more CTAs per block) for small batches.
-  const int wt_total = D / 256;
-  const long long want = 2ll * sms;
-  int per = static_cast<int>((static_cast<long long>(wt_total) * max_blocks + want - 1) / want);
-  if (per < 1) per = 1;
-  if (per > wt_total) per = wt_total;
-  a.tiles_per_cta = per;
-  const int groups = (wt_total + per - 1) / per;
+  // one CTA per SM, or one per unit when the blocks can give fewer units
+  const long long max_units = static_cast<long long>(max_blocks) * (D / 256);
+  const int grid = static_cast<int>(max_units < sms ? max_units : sms);
+  if (grid < 1) return 0;
   static std::atomic<unsigned long long> attr_devs{0};
   if (ensure_func_attrs(attr_devs, [&] {
         return cudaFuncSetAttribute(a4w4_moe2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kM2Smem) ==
@@ -266,7 +333,7 @@ int launch_moe_gemm2_resident(const void* Aq, const void* As, int T, int I, cons
       }) != 0)
     return -4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(groups), static_cast<unsigned>(max_blocks), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kM2Threads, 1, 1);
   cfg.dynamicSmemBytes = kM2Smem;
   cfg.stream = st;
