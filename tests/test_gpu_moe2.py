@@ -166,10 +166,13 @@ def run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb):
     return host_bits(Y)
 
 
-@pytest.mark.parametrize("T,E,topk", [(21, 6, 3),      # few rows per expert: resident-activation kernel
-                                       (200, 4, 2)])    # many: one CTA per (block, column tile)
-def test_gemm2_small_every_output(T, E, topk):
-    D, I = 512, 256
+@pytest.mark.parametrize("T,E,topk,D,I", [
+    (21, 6, 3, 512, 256),       # few rows per expert, one CTA per unit
+    (200, 4, 2, 512, 256),      # experts with more than one 128-row block
+    (37, 5, 2, 256, 1024),      # one column tile per block; I = 1024, the largest K (4 tiles resident)
+    (600, 8, 4, 3584, 256),     # 378 units over 152 CTAs: runs that cross block boundaries
+], ids=lambda v: str(v))
+def test_gemm2_small_every_output(T, E, topk, D, I):
     ids = workloads.moe_topk_ids(T, E, topk)
     wts = workloads.moe_topk_weights(T, topk)
     H = workloads.moe_hidden_bits(T * topk, I)
