@@ -81,8 +81,9 @@ def test_ragged_m_spans_tiles(M):
                                    # large-M tiles without split-K: one K tile; K range longer than the ring
                                    (256, 512, 256), (1024, 5120, 1536),
                                    # persistent large-M walk: two tiles per CTA and a ragged last row
-                                   # tile; a last partial wave run as 128-column halves after a full tile
-                                   (1100, 8192, 512), (1200, 4096, 512)])
+                                   # tile; a last partial wave run as 128-column halves after a full tile;
+                                   # K = 128, one K tile half of which is padding
+                                   (1100, 8192, 512), (1200, 4096, 512), (1100, 8192, 128)])
 def test_k_tails_and_shapes(M, N, K):
     A, W = workloads.dense_problem(M, N, K, "large", seed=K)
     check_full(A, W)

@@ -200,7 +200,8 @@ def full_w2():
 @pytest.mark.parametrize("T", CFG["tokens"])
 def test_gemm2_workload(T, full_w2):
     """The MoE workload shape at full size for every token count; the oracle
-    checks every output of up to 4 sampled tokens (all for T = 1)."""
+    checks every output of up to 4 sampled tokens (all for T = 1), and a
+    second run gives the same bits for every token."""
     W2q, W2s = full_w2
     E, topk, D, I = E_FULL, TOPK_FULL, D_FULL, I_FULL
     ids = workloads.moe_topk_ids(T, E, topk)
@@ -210,8 +211,10 @@ def test_gemm2_workload(T, full_w2):
     rows, bexp, nb = run_sort(ids, E)
     er, _, enb = moe.sort_routed_rows(ids, E, 128)
     tq, ts = gemm2_tiles(q, s, er, enb, T * topk, I)
-    y_gpu = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, a4w4.a4w4_moe_max_blocks(T, topk, E, 128))
+    maxb = a4w4.a4w4_moe_max_blocks(T, topk, E, 128)
+    y_gpu = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
     assert np.all((y_gpu & 0x7F80) != 0x7F80), "NaN or Inf in the output"
+    assert np.array_equal(y_gpu, run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb))
     tokens = np.arange(T) if T == 1 else np.random.default_rng(T).choice(T, 4, replace=False)
     y, abs_sum, _ = moe.gemm2_tokens(q, s, ids, wts, lambda e: workloads.moe_expert_w2_bits(e, D, I), tokens)
     bad = gemm_violations(y_gpu[tokens], y, abs_sum)[0]
@@ -256,7 +259,7 @@ def test_two_stages_chained(act):
 @pytest.mark.parametrize("T,E,topk", [(21, 6, 3), (200, 4, 2)])
 def test_gemm2_bitwise_deterministic(T, E, topk):
     """Each routed row is written by one CTA and a token's rows are summed in k
-    order (both GEMM2 kernels): repeated runs agree bit for bit."""
+    order: repeated runs agree bit for bit."""
     D, I = 512, 256
     ids = workloads.moe_topk_ids(T, E, topk)
     wts = workloads.moe_topk_weights(T, topk)
