@@ -96,3 +96,28 @@ def test_a16w4_bitwise_deterministic(M, N, K):
     c1 = run(A, W)
     c2 = run(A, W)
     assert np.array_equal(c1, c2)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 7168, 4224), (32, 1536, 7168)])
+def test_a16w4_expired_wait_is_reported_and_context_survives(M, N, K):
+    """With a 1 ns wait limit the kernel's waits expire: it reports
+    A4W4_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns; the
+    next call with the default limit gives the same bits as a normal run."""
+    A, W = workloads.dense_problem(M, N, K, "decode")
+    want = run(A, W)
+    Wq = torch.empty(a4w4.a4w4_weight_codes_bytes(N, K), dtype=torch.uint8, device="cuda")
+    Ws = torch.empty(a4w4.a4w4_weight_scales_bytes(N, K), dtype=torch.uint8, device="cuda")
+    a4w4.a4w4_prepare_gemm_weight(dev_bits(W), N, K, Wq, Ws)
+    C = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    assert a4w4.a4w4_get_device_status() == 0
+    a4w4.a4w4_set_wait_limit_ns(1)
+    try:
+        a4w4.a4w4_gemm_a16w4(dev_bits(A), M, K, Wq, Ws, N, C, 0)
+        status = a4w4.a4w4_get_device_status()
+    finally:
+        a4w4.a4w4_set_wait_limit_ns(0)
+    assert status == a4w4.A4W4_ERR_TIMEOUT
+    assert a4w4.a4w4_get_device_status() == 0
+    a4w4.a4w4_gemm_a16w4(dev_bits(A), M, K, Wq, Ws, N, C, 0)
+    assert a4w4.a4w4_get_device_status() == 0
+    assert np.array_equal(C.cpu().numpy().view(np.uint16), want)

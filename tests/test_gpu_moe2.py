@@ -275,3 +275,42 @@ def test_gemm2_bitwise_deterministic(T, E, topk):
     y1 = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
     y2 = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
     assert np.array_equal(y1, y2)
+
+
+def test_gemm2_expired_wait_is_reported_and_context_survives():
+    """With a 1 ns wait limit the persistent walk's waits expire: it reports
+    A4W4_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and returns; the
+    next call with the default limit gives the same bits as a normal run."""
+    T, E, topk, D, I = 600, 8, 4, 3584, 256
+    ids = workloads.moe_topk_ids(T, E, topk)
+    wts = workloads.moe_topk_weights(T, topk)
+    q, s = mxfp4.mxfp4_quant(workloads.moe_hidden_bits(T * topk, I))
+    W2 = np.concatenate([workloads.moe_expert_w2_bits(e, D, I) for e in range(E)])
+    W2q = torch.empty(E * a4w4.a4w4_weight_codes_bytes(D, I), dtype=torch.uint8, device="cuda")
+    W2s = torch.empty(E * a4w4.a4w4_weight_scales_bytes(D, I), dtype=torch.uint8, device="cuda")
+    a4w4.a4w4_prepare_gemm_weight(dev_bits(W2), E * D, I, W2q, W2s)
+    rows, bexp, nb = run_sort(ids, E)
+    er, _, enb = moe.sort_routed_rows(ids, E, 128)
+    tq, ts = gemm2_tiles(q, s, er, enb, T * topk, I)
+    maxb = a4w4.a4w4_moe_max_blocks(T, topk, E, 128)
+    want = run_gemm2(tq, ts, T, I, rows, bexp, nb, topk, wts, W2q, W2s, E, D, maxb)
+    Aq = torch.zeros(maxb * (I // 256) * 16384, dtype=torch.uint8, device="cuda")
+    As = torch.zeros(maxb * (I // 256) * 1024, dtype=torch.uint8, device="cuda")
+    Aq[:tq.size].copy_(torch.from_numpy(tq))
+    As[:ts.size].copy_(torch.from_numpy(ts))
+    wsb = a4w4.a4w4_moe_gemm2_workspace_bytes(T, topk, D)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    w_dev = torch.from_numpy(wts).cuda()
+    assert a4w4.a4w4_get_device_status() == 0
+    a4w4.a4w4_set_wait_limit_ns(1)
+    try:
+        a4w4.a4w4_moe_gemm2(Aq, As, T, I, rows, bexp, nb, topk, w_dev, W2q, W2s, E, D, Y, ws, wsb)
+        status = a4w4.a4w4_get_device_status()
+    finally:
+        a4w4.a4w4_set_wait_limit_ns(0)
+    assert status == a4w4.A4W4_ERR_TIMEOUT
+    assert a4w4.a4w4_get_device_status() == 0
+    a4w4.a4w4_moe_gemm2(Aq, As, T, I, rows, bexp, nb, topk, w_dev, W2q, W2s, E, D, Y, ws, wsb)
+    assert a4w4.a4w4_get_device_status() == 0
+    assert np.array_equal(host_bits(Y), want)
