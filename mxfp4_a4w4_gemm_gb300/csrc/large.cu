@@ -10,7 +10,11 @@
 // the last, partial wave (two CTAs take the two halves: the wave's operand
 // bytes per SM drop from 51 KB to 34 KB per K step, its own output columns
 // each, nothing to reduce).  The operand ring runs on across units: the next
-// unit's copies land while the epilogue drains the accumulator.
+// unit's copies land while the epilogue drains the accumulator.  The ring's
+// 204 KB hold four 51 KB stages of whole tiles or six 34 KB stages of halves
+// (a half unit's stage is not bound by the SM's intake but by how many bytes
+// are in flight); a CTA whose walk goes on from whole tiles to halves lets
+// the whole-tile stages drain before it reuses their bytes.
 //   warp 0     producer: per 256-wide K step one 17 KB activation atom, the
 //              two adjacent 16 KB weight atoms and their 2 KB of scales (one
 //              atom and 1 KB for a half unit);
@@ -39,24 +43,20 @@ struct LargeArgs {
   unsigned int* status;
 };
 
-constexpr int kLargeStages = 4;
-
 struct LCfg {
-  static constexpr int STAGES = kLargeStages;
   static constexpr int THREADS = 192;
   static constexpr int A_BYTES = 17408;          // 128 rows x 256 K: codes + scales
-  static constexpr int W_BYTES = 32768;          // two 128-row weight atoms
-  static constexpr int WSF_BYTES = 2048;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_W = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_WSF = OFF_W + STAGES * W_BYTES;
+  static constexpr int ATOM_BYTES = 16384;       // one 128-row weight atom, one K step
+  static constexpr int ATOM_SF_BYTES = 1024;     // its scales
+  static constexpr int RING_BYTES = 4 * (A_BYTES + 2 * (ATOM_BYTES + ATOM_SF_BYTES));
   // epilogue turnaround: per warp 32 rows x 64 BF16 columns, rows padded to
   // 144 bytes (conflict-free 16-byte accesses row-wise and column-wise)
   static constexpr int STG_PITCH = 144;
   static constexpr int STG_BYTES = 32 * STG_PITCH;
-  static constexpr int OFF_STG = OFF_WSF + STAGES * WSF_BYTES;
+  static constexpr int OFF_STG = RING_BYTES;
   static constexpr int OFF_BAR = OFF_STG + 4 * STG_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 3;    // full, empty per stage; acc_full, acc_empty, drain
+  // full, empty per stage of the two rings; acc_full, acc_empty, drain
+  static constexpr int NBAR = 2 * (4 + 6) + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int ACC_COLS = 256;
@@ -64,10 +64,32 @@ struct LCfg {
   static constexpr int SFB_COLS = 16;            // 2 K halves x 2 weight atoms x 4 columns
   static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
   static constexpr int TMEM_COLS = 512;
-  static_assert(A_BYTES % 1024 == 0 && W_BYTES % 1024 == 0, "swizzled tiles start 1024-aligned");
-  static_assert(ACC_COLS + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+
+// The two ring geometries over the same bytes.  Each keeps the activation
+// atoms, the weight atoms and the weight scales of all its stages in three
+// separate arrays (activation atoms first); barriers BAR .. BAR+STAGES-1 are
+// the stages' "landed" barriers, the next STAGES their "consumed" ones.
+template <bool HALF>
+struct LRing {
+  static constexpr int STAGES = HALF ? 6 : 4;
+  static constexpr int ATOMS = HALF ? 1 : 2;     // weight atoms per stage
+  static constexpr int W_BYTES = ATOMS * LCfg::ATOM_BYTES;
+  static constexpr int WSF_BYTES = ATOMS * LCfg::ATOM_SF_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_W = OFF_A + STAGES * LCfg::A_BYTES;
+  static constexpr int OFF_WSF = OFF_W + STAGES * W_BYTES;
+  static constexpr int BAR = HALF ? 8 : 0;
+  static constexpr uint32_t TX = LCfg::A_BYTES + W_BYTES + WSF_BYTES;
+  static_assert(LCfg::A_BYTES % 1024 == 0 && OFF_W % 1024 == 0 && W_BYTES % 1024 == 0,
+                "swizzled tiles start 1024-aligned");
+  static_assert(OFF_WSF + STAGES * WSF_BYTES <= LCfg::RING_BYTES, "ring bytes");
+  static_assert(LCfg::ACC_COLS + STAGES * LCfg::SF_STAGE_COLS <= LCfg::TMEM_COLS, "TMEM budget");
+  static __device__ __forceinline__ uint32_t full(uint32_t bar0, int s) { return bar0 + 8u * (BAR + s); }
+  static __device__ __forceinline__ uint32_t empty(uint32_t bar0, int s) { return bar0 + 8u * (BAR + STAGES + s); }
+};
+static_assert(6 * 34816 <= LCfg::RING_BYTES, "six half-unit stages fit the four whole-tile stages' bytes");
 
 // Unit u -> tile and column half (-1: the whole 256 columns).
 __device__ __forceinline__ void large_unit(const LargeArgs& p, int u, int& tile, int& half) {
@@ -86,9 +108,65 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Producer: the K steps of one unit into ring R; g counts the stages issued
+// on R.  False when a wait gave up.
+template <bool HALF>
+__device__ __forceinline__ bool large_produce(const LargeArgs& p, uint32_t base, uint32_t bar0, int tile, int half,
+                                              int& g, uint64_t pol, volatile int* abort_flag) {
+  using R = LRing<HALF>;
+  const int x_tile = tile / p.w_tiles, w_tile = tile % p.w_tiles;
+  for (int kt = 0; kt < p.KT; ++kt) {
+    const int s = g % R::STAGES;
+    if (!mbar_wait(R::empty(bar0, s), ((g / R::STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) return false;
+    const long long aatom = static_cast<long long>(x_tile) * p.KT + kt;
+    const long long watom = weight_atom(2 * w_tile, kt, p.KT) + (half > 0 ? 1 : 0);
+    const uint32_t fb = R::full(bar0, s);
+    mbar_arrive_expect_tx(fb, R::TX);
+    bulk_g2s(base + R::OFF_A + s * LCfg::A_BYTES, p.Aq + aatom * LCfg::A_BYTES, LCfg::A_BYTES, fb, pol);
+    bulk_g2s(base + R::OFF_W + s * R::W_BYTES, p.Wq + watom * LCfg::ATOM_BYTES, R::W_BYTES, fb, pol);
+    bulk_g2s(base + R::OFF_WSF + s * R::WSF_BYTES, p.Ws + watom * LCfg::ATOM_SF_BYTES, R::WSF_BYTES, fb, pol);
+    ++g;
+  }
+  return true;
+}
+
+// MMA issuer: the K steps of one unit from ring R into the accumulator.
+template <bool HALF>
+__device__ __forceinline__ bool large_mma(const LargeArgs& p, uint32_t base, uint32_t bar0, uint32_t tmem, int& g,
+                                          volatile int* abort_flag) {
+  using R = LRing<HALF>;
+  constexpr int N = HALF ? 128 : 256;
+  const uint32_t idesc0 = idesc_mxf4(N, 0, 0), idesc2 = idesc_mxf4(N, 2, 2);
+  const uint64_t adesc0 = sdesc_sw128(base + R::OFF_A), bdesc0 = sdesc_sw128(base + R::OFF_W);
+  const uint64_t asfd0 = sdesc_sf(base + R::OFF_A + 16384), bsfd0 = sdesc_sf(base + R::OFF_WSF);
+  for (int kt = 0; kt < p.KT; ++kt) {
+    const int s = g % R::STAGES;
+    if (!mbar_wait(R::full(bar0, s), (g / R::STAGES) & 1u, abort_flag, p.wait_ns, p.status)) return false;
+    tc_fence_after();
+    const uint32_t sfa = tmem + LCfg::ACC_COLS + s * LCfg::SF_STAGE_COLS;
+    const uint32_t sfb = sfa + LCfg::SFA_COLS;
+    const uint64_t ad = adesc0 + ((s * LCfg::A_BYTES) >> 4), bd = bdesc0 + ((s * R::W_BYTES) >> 4);
+    const uint64_t asd = asfd0 + ((s * LCfg::A_BYTES) >> 4), bsd = bsfd0 + ((s * R::WSF_BYTES) >> 4);
+#pragma unroll
+    for (int ka = 0; ka < 2; ++ka) {
+      tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
+      tmem_copy_sf_desc(sfb + ka * 8, bsd + (ka * 512) / 16);
+      if (!HALF) tmem_copy_sf_desc(sfb + ka * 8 + 4, bsd + (1024 + ka * 512) / 16);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const int ka = ks >> 1;
+      mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4, sfb + ka * 8,
+               (kt > 0 || ks > 0) ? 1u : 0u);
+    }
+    mma_commit(R::empty(bar0, s));
+    ++g;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const LargeArgs p) {
   using Cf = LCfg;
-  constexpr int STAGES = Cf::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -98,9 +176,7 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
   const unsigned long long drain_ns = p.wait_ns > 100000000ull ? p.wait_ns : 100000000ull;
 
   const uint32_t bar0 = base + Cf::OFF_BAR;
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  const uint32_t acc_full = bar0 + 8u * (2 * STAGES);    // a unit's accumulator is complete
+  const uint32_t acc_full = bar0 + 8u * (Cf::NBAR - 3);   // a unit's accumulator is complete
   const uint32_t acc_empty = acc_full + 8u;               // the epilogue has read it
   const uint32_t drain = acc_empty + 8u;                  // every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cf::OFF_MISC);
@@ -108,10 +184,7 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cf::OFF_MISC + 16);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
-    }
+    for (int b = 0; b < Cf::NBAR - 3; ++b) mbar_init(bar0 + 8u * b, 1);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 128);
     mbar_init(drain, 1);
@@ -134,78 +207,46 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
     // ---------------- producer ----------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();   // operands are re-read by other tiles from L2
-      int g = 0;                                  // stages issued (the ring runs on across units)
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += G) {
-        int tile, half;
-        large_unit(p, u, tile, half);
-        const int x_tile = tile / p.w_tiles, w_tile = tile % p.w_tiles;
-        const int atoms = half < 0 ? 2 : 1;
-        const uint32_t bytes = Cf::A_BYTES + atoms * (16384 + 1024);
-        for (int kt = 0; kt < p.KT; ++kt) {
-          const int s = g % STAGES;
-          if (!mbar_wait(empty(s), ((g / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          const long long aatom = static_cast<long long>(x_tile) * p.KT + kt;
-          const long long watom = weight_atom(2 * w_tile, kt, p.KT) + (half > 0 ? 1 : 0);
-          mbar_arrive_expect_tx(full(s), bytes);
-          bulk_g2s(base + Cf::OFF_A + s * Cf::A_BYTES, p.Aq + aatom * Cf::A_BYTES, Cf::A_BYTES, full(s), pol);
-          bulk_g2s(base + Cf::OFF_W + s * Cf::W_BYTES, p.Wq + watom * 16384, atoms * 16384, full(s), pol);
-          bulk_g2s(base + Cf::OFF_WSF + s * Cf::WSF_BYTES, p.Ws + watom * 1024, atoms * 1024, full(s), pol);
-          ++g;
+      int g = 0, gh = 0;                          // stages issued on each ring (a ring runs on across units)
+      bool ok = true, on_half = false;
+      int u = blockIdx.x;
+      for (; u < p.full_units && ok; u += G) ok = large_produce<false>(p, base, bar0, u, -1, g, pol, abort_flag);
+      if (ok && u < p.units) {
+        // the half-unit ring reuses the whole-tile ring's bytes: every
+        // whole-tile stage issued has been consumed first
+        for (int j = (g > 4 ? g - 4 : 0); j < g && ok; ++j)
+          ok = mbar_wait(LRing<false>::empty(bar0, j % 4), (j / 4) & 1u, abort_flag, p.wait_ns, p.status);
+        on_half = ok;
+        for (; u < p.units && ok; u += G) {
+          int tile, half;
+          large_unit(p, u, tile, half);
+          ok = large_produce<true>(p, base, bar0, tile, half, gh, pol, abort_flag);
         }
       }
       // every copy issued lands before the CTA's shared memory is released
-      for (int j = (g > STAGES ? g - STAGES : 0); j < g; ++j)
-        mbar_wait(full(j % STAGES), (j / STAGES) & 1u, never, drain_ns, p.status);
+      if (on_half) {
+        for (int j = (gh > 6 ? gh - 6 : 0); j < gh; ++j)
+          mbar_wait(LRing<true>::full(bar0, j % 6), (j / 6) & 1u, never, drain_ns, p.status);
+      } else {
+        for (int j = (g > 4 ? g - 4 : 0); j < g; ++j)
+          mbar_wait(LRing<false>::full(bar0, j % 4), (j / 4) & 1u, never, drain_ns, p.status);
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // (a half stage's scales reuse a whole-tile stage's TMEM columns only
+    // after the producer has seen every whole-tile stage consumed)
     if (lane == 0) {
-      const uint64_t adesc0 = sdesc_sw128(base + Cf::OFF_A), bdesc0 = sdesc_sw128(base + Cf::OFF_W);
-      const uint64_t asfd0 = sdesc_sf(base + Cf::OFF_A + 16384), bsfd0 = sdesc_sf(base + Cf::OFF_WSF);
-      const uint32_t id_full0 = idesc_mxf4(256, 0, 0), id_full2 = idesc_mxf4(256, 2, 2);
-      const uint32_t id_half0 = idesc_mxf4(128, 0, 0), id_half2 = idesc_mxf4(128, 2, 2);
-      const uint32_t sf_col0 = tmem + Cf::ACC_COLS;
-      int g = 0, j = 0;
+      int g = 0, gh = 0, j = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += G, ++j) {
-        int tile, half;
-        large_unit(p, u, tile, half);
         // the epilogue has read the previous unit's accumulator
         if (j > 0) {
           if (!mbar_wait(acc_empty, static_cast<uint32_t>((j - 1) & 1), abort_flag, p.wait_ns, p.status)) break;
           tc_fence_after();
         }
-        const uint32_t idesc0 = half < 0 ? id_full0 : id_half0, idesc2 = half < 0 ? id_full2 : id_half2;
-        for (int kt = 0; kt < p.KT; ++kt) {
-          const int s = g % STAGES;
-          if (!mbar_wait(full(s), (g / STAGES) & 1u, abort_flag, p.wait_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sfa = sf_col0 + s * Cf::SF_STAGE_COLS;
-          const uint32_t sfb = sfa + Cf::SFA_COLS;
-          const uint64_t ad = adesc0 + ((s * Cf::A_BYTES) >> 4), bd = bdesc0 + ((s * Cf::W_BYTES) >> 4);
-          const uint64_t asd = asfd0 + ((s * Cf::A_BYTES) >> 4), bsd = bsfd0 + ((s * Cf::WSF_BYTES) >> 4);
-#pragma unroll
-          for (int ka = 0; ka < 2; ++ka) {
-            tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
-            tmem_copy_sf_desc(sfb + ka * 8, bsd + (ka * 512) / 16);
-            if (half < 0) tmem_copy_sf_desc(sfb + ka * 8 + 4, bsd + (1024 + ka * 512) / 16);
-          }
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const int ka = ks >> 1;
-            mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4, sfb + ka * 8,
-                     (kt > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(empty(s));
-          ++g;
-        }
+        ok = u < p.full_units ? large_mma<false>(p, base, bar0, tmem, g, abort_flag)
+                              : large_mma<true>(p, base, bar0, tmem, gh, abort_flag);
         if (ok) mma_commit(acc_full);
       }
       // TMEM is released only after every MMA issued has completed.
