@@ -650,10 +650,11 @@ def measure(name, args, wl, desc, torch, stream, dev, world, barrier, peaks, pea
              "tflops": round(world * wl.flops_per_step / (ms_per_step * 1e-3) / 1e12, 2),
              "gemms_per_step": len(wl.shapes), "per_gemm": per, "roofline": roof_hbm,
              "timed_regions": nregions, "clocks": clk.summary()}
-    if name == "large":
+    big = [p for p in per if p["M"] >= 512] if name == "large" else []
+    if big:
         # the compute-bound end of the metric: FP4 tensor roofline over the
-        # GEMMs with M >= 512, the dominant kernel's launches
-        big = [p for p in per if p["M"] >= 512]
+        # GEMMs with M >= 512, the dominant kernel's launches (a --shape run
+        # below 512 rows keeps the HBM roofline)
         us = sum(p["us"] for p in big)
         fl = sum(p["flops"] for p in big)
         tf = fl / (us * 1e-6) / 1e12
