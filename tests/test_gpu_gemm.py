@@ -82,8 +82,11 @@ def test_ragged_m_spans_tiles(M):
                                    (256, 512, 256), (1024, 5120, 1536),
                                    # persistent large-M walk: two tiles per CTA and a ragged last row
                                    # tile; a last partial wave run as 128-column halves after a full tile;
-                                   # K = 128, one K tile half of which is padding
-                                   (1100, 8192, 512), (1200, 4096, 512), (1100, 8192, 128)])
+                                   # K = 128, one K tile half of which is padding; the switch from the
+                                   # 4-deep whole-tile ring to the 6-deep half-unit ring after 5 K tiles
+                                   # (not a multiple of either depth)
+                                   (1100, 8192, 512), (1200, 4096, 512), (1100, 8192, 128),
+                                   (1200, 4096, 1280)])
 def test_k_tails_and_shapes(M, N, K):
     A, W = workloads.dense_problem(M, N, K, "large", seed=K)
     check_full(A, W)
