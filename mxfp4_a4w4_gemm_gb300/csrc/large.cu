@@ -11,13 +11,15 @@
 // bytes per SM drop from 51 KB to 34 KB per K step, its own output columns
 // each, nothing to reduce).  The operand ring runs on across units: the next
 // unit's copies land while the epilogue drains the accumulator.  The ring's
-// 204 KB hold four 51 KB stages of whole tiles or six 34 KB stages of halves
-// (a half unit's stage is not bound by the SM's intake but by how many bytes
-// are in flight); a CTA whose walk goes on from whole tiles to halves lets
-// the whole-tile stages drain before it reuses their bytes.
+// 204 KB hold four 51 KB stages of one K step for whole tiles, or three 68 KB
+// stages of two K steps for halves (the SM's bulk-copy pipe turns a stage
+// over in no less than ~0.42 us whatever its size up to ~51 KB, so a half
+// unit's 34 KB per K step would leave it a third idle); a CTA whose walk goes
+// on from whole tiles to halves lets the whole-tile stages drain before it
+// reuses their bytes.
 //   warp 0     producer: per 256-wide K step one 17 KB activation atom, the
 //              two adjacent 16 KB weight atoms and their 2 KB of scales (one
-//              atom and 1 KB for a half unit);
+//              atom and 1 KB for a half unit, two K steps to a stage);
 //   warp 1     TMEM owner and MMA issuer: scale copies into TMEM, four
 //              tcgen05.mma.kind::mxf4.block_scale (M = 128, N = 256 or 128,
 //              K = 64) per step; before a unit's first MMA it waits until the
@@ -56,7 +58,7 @@ struct LCfg {
   static constexpr int OFF_STG = RING_BYTES;
   static constexpr int OFF_BAR = OFF_STG + 4 * STG_BYTES;
   // full, empty per stage of the two rings; acc_full, acc_empty, drain
-  static constexpr int NBAR = 2 * (4 + 6) + 3;
+  static constexpr int NBAR = 2 * (4 + 3) + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int ACC_COLS = 256;
@@ -67,29 +69,37 @@ struct LCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// The two ring geometries over the same bytes.  Each keeps the activation
-// atoms, the weight atoms and the weight scales of all its stages in three
-// separate arrays (activation atoms first); barriers BAR .. BAR+STAGES-1 are
-// the stages' "landed" barriers, the next STAGES their "consumed" ones.
+// The two ring geometries over the same bytes.  A stage holds KTS K steps:
+// their activation atoms side by side (consecutive K steps of a row tile are
+// adjacent in the activation tiles, one copy), then per K step the weight
+// atom(s) and their scales; each geometry keeps the activation, weight and
+// scale parts of all its stages in three separate arrays.  Barriers BAR ..
+// BAR+STAGES-1 are the stages' "landed" barriers, the next STAGES their
+// "consumed" ones.
 template <bool HALF>
 struct LRing {
-  static constexpr int STAGES = HALF ? 6 : 4;
-  static constexpr int ATOMS = HALF ? 1 : 2;     // weight atoms per stage
-  static constexpr int W_BYTES = ATOMS * LCfg::ATOM_BYTES;
-  static constexpr int WSF_BYTES = ATOMS * LCfg::ATOM_SF_BYTES;
+  static constexpr int STAGES = HALF ? 3 : 4;
+  static constexpr int KTS = HALF ? 2 : 1;       // K steps per stage
+  static constexpr int ATOMS = HALF ? 1 : 2;     // weight atoms per K step
+  static constexpr int W_STEP = ATOMS * LCfg::ATOM_BYTES;
+  static constexpr int WSF_STEP = ATOMS * LCfg::ATOM_SF_BYTES;
+  static constexpr int A_STAGE = KTS * LCfg::A_BYTES;
+  static constexpr int W_STAGE = KTS * W_STEP;
+  static constexpr int WSF_STAGE = KTS * WSF_STEP;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_W = OFF_A + STAGES * LCfg::A_BYTES;
-  static constexpr int OFF_WSF = OFF_W + STAGES * W_BYTES;
+  static constexpr int OFF_W = OFF_A + STAGES * A_STAGE;
+  static constexpr int OFF_WSF = OFF_W + STAGES * W_STAGE;
   static constexpr int BAR = HALF ? 8 : 0;
-  static constexpr uint32_t TX = LCfg::A_BYTES + W_BYTES + WSF_BYTES;
-  static_assert(LCfg::A_BYTES % 1024 == 0 && OFF_W % 1024 == 0 && W_BYTES % 1024 == 0,
+  static constexpr uint32_t TX_STEP = LCfg::A_BYTES + W_STEP + WSF_STEP;   // bytes per K step
+  static_assert(LCfg::A_BYTES % 1024 == 0 && OFF_W % 1024 == 0 && W_STEP % 1024 == 0,
                 "swizzled tiles start 1024-aligned");
-  static_assert(OFF_WSF + STAGES * WSF_BYTES <= LCfg::RING_BYTES, "ring bytes");
-  static_assert(LCfg::ACC_COLS + STAGES * LCfg::SF_STAGE_COLS <= LCfg::TMEM_COLS, "TMEM budget");
+  static_assert(OFF_WSF + STAGES * WSF_STAGE <= LCfg::RING_BYTES, "ring bytes");
+  static_assert(LCfg::ACC_COLS + STAGES * KTS * LCfg::SF_STAGE_COLS <= LCfg::TMEM_COLS, "TMEM budget");
   static __device__ __forceinline__ uint32_t full(uint32_t bar0, int s) { return bar0 + 8u * (BAR + s); }
   static __device__ __forceinline__ uint32_t empty(uint32_t bar0, int s) { return bar0 + 8u * (BAR + STAGES + s); }
 };
-static_assert(6 * 34816 <= LCfg::RING_BYTES, "six half-unit stages fit the four whole-tile stages' bytes");
+static_assert(LRing<true>::BAR == 2 * LRing<false>::STAGES, "barrier layout");
+static_assert(2 * (LRing<false>::STAGES + LRing<true>::STAGES) + 3 == LCfg::NBAR, "barrier count");
 
 // Unit u -> tile and column half (-1: the whole 256 columns).
 __device__ __forceinline__ void large_unit(const LargeArgs& p, int u, int& tile, int& half) {
@@ -108,23 +118,28 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Producer: the K steps of one unit into ring R; g counts the stages issued
-// on R.  False when a wait gave up.
+// Producer: the K steps of one unit into ring R, KTS per stage (fewer in the
+// last stage when KT is not a multiple); g counts the stages issued on R.
+// False when a wait gave up.
 template <bool HALF>
 __device__ __forceinline__ bool large_produce(const LargeArgs& p, uint32_t base, uint32_t bar0, int tile, int half,
                                               int& g, uint64_t pol, volatile int* abort_flag) {
   using R = LRing<HALF>;
   const int x_tile = tile / p.w_tiles, w_tile = tile % p.w_tiles;
-  for (int kt = 0; kt < p.KT; ++kt) {
+  for (int kt = 0; kt < p.KT; kt += R::KTS) {
+    const int nk = p.KT - kt < R::KTS ? p.KT - kt : R::KTS;
     const int s = g % R::STAGES;
     if (!mbar_wait(R::empty(bar0, s), ((g / R::STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) return false;
     const long long aatom = static_cast<long long>(x_tile) * p.KT + kt;
-    const long long watom = weight_atom(2 * w_tile, kt, p.KT) + (half > 0 ? 1 : 0);
     const uint32_t fb = R::full(bar0, s);
-    mbar_arrive_expect_tx(fb, R::TX);
-    bulk_g2s(base + R::OFF_A + s * LCfg::A_BYTES, p.Aq + aatom * LCfg::A_BYTES, LCfg::A_BYTES, fb, pol);
-    bulk_g2s(base + R::OFF_W + s * R::W_BYTES, p.Wq + watom * LCfg::ATOM_BYTES, R::W_BYTES, fb, pol);
-    bulk_g2s(base + R::OFF_WSF + s * R::WSF_BYTES, p.Ws + watom * LCfg::ATOM_SF_BYTES, R::WSF_BYTES, fb, pol);
+    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nk) * R::TX_STEP);
+    bulk_g2s(base + R::OFF_A + s * R::A_STAGE, p.Aq + aatom * LCfg::A_BYTES, nk * LCfg::A_BYTES, fb, pol);
+    for (int k2 = 0; k2 < nk; ++k2) {
+      const long long watom = weight_atom(2 * w_tile, kt + k2, p.KT) + (half > 0 ? 1 : 0);
+      bulk_g2s(base + R::OFF_W + s * R::W_STAGE + k2 * R::W_STEP, p.Wq + watom * LCfg::ATOM_BYTES, R::W_STEP, fb, pol);
+      bulk_g2s(base + R::OFF_WSF + s * R::WSF_STAGE + k2 * R::WSF_STEP, p.Ws + watom * LCfg::ATOM_SF_BYTES,
+               R::WSF_STEP, fb, pol);
+    }
     ++g;
   }
   return true;
@@ -139,25 +154,32 @@ __device__ __forceinline__ bool large_mma(const LargeArgs& p, uint32_t base, uin
   const uint32_t idesc0 = idesc_mxf4(N, 0, 0), idesc2 = idesc_mxf4(N, 2, 2);
   const uint64_t adesc0 = sdesc_sw128(base + R::OFF_A), bdesc0 = sdesc_sw128(base + R::OFF_W);
   const uint64_t asfd0 = sdesc_sf(base + R::OFF_A + 16384), bsfd0 = sdesc_sf(base + R::OFF_WSF);
-  for (int kt = 0; kt < p.KT; ++kt) {
+  for (int kt = 0; kt < p.KT; kt += R::KTS) {
+    const int nk = p.KT - kt < R::KTS ? p.KT - kt : R::KTS;
     const int s = g % R::STAGES;
     if (!mbar_wait(R::full(bar0, s), (g / R::STAGES) & 1u, abort_flag, p.wait_ns, p.status)) return false;
     tc_fence_after();
-    const uint32_t sfa = tmem + LCfg::ACC_COLS + s * LCfg::SF_STAGE_COLS;
-    const uint32_t sfb = sfa + LCfg::SFA_COLS;
-    const uint64_t ad = adesc0 + ((s * LCfg::A_BYTES) >> 4), bd = bdesc0 + ((s * R::W_BYTES) >> 4);
-    const uint64_t asd = asfd0 + ((s * LCfg::A_BYTES) >> 4), bsd = bsfd0 + ((s * R::WSF_BYTES) >> 4);
 #pragma unroll
-    for (int ka = 0; ka < 2; ++ka) {
-      tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
-      tmem_copy_sf_desc(sfb + ka * 8, bsd + (ka * 512) / 16);
-      if (!HALF) tmem_copy_sf_desc(sfb + ka * 8 + 4, bsd + (1024 + ka * 512) / 16);
-    }
+    for (int k2 = 0; k2 < R::KTS; ++k2) {
+      if (k2 < nk) {
+        const uint32_t sfa = tmem + LCfg::ACC_COLS + (s * R::KTS + k2) * LCfg::SF_STAGE_COLS;
+        const uint32_t sfb = sfa + LCfg::SFA_COLS;
+        const uint32_t aoff = s * R::A_STAGE + k2 * LCfg::A_BYTES;
+        const uint64_t ad = adesc0 + (aoff >> 4), bd = bdesc0 + ((s * R::W_STAGE + k2 * R::W_STEP) >> 4);
+        const uint64_t asd = asfd0 + (aoff >> 4), bsd = bsfd0 + ((s * R::WSF_STAGE + k2 * R::WSF_STEP) >> 4);
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int ka = ks >> 1;
-      mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4, sfb + ka * 8,
-               (kt > 0 || ks > 0) ? 1u : 0u);
+        for (int ka = 0; ka < 2; ++ka) {
+          tmem_copy_sf_desc(sfa + ka * 4, asd + ka * (512 >> 4));
+          tmem_copy_sf_desc(sfb + ka * 8, bsd + (ka * 512) / 16);
+          if (!HALF) tmem_copy_sf_desc(sfb + ka * 8 + 4, bsd + (1024 + ka * 512) / 16);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const int ka = ks >> 1;
+          mma_mxf4(tmem, ad + ks * 2, bd + ks * 2, (ks & 1) ? idesc2 : idesc0, sfa + ka * 4, sfb + ka * 8,
+                   (kt + k2 > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
     }
     mma_commit(R::empty(bar0, s));
     ++g;
@@ -214,8 +236,9 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
       if (ok && u < p.units) {
         // the half-unit ring reuses the whole-tile ring's bytes: every
         // whole-tile stage issued has been consumed first
-        for (int j = (g > 4 ? g - 4 : 0); j < g && ok; ++j)
-          ok = mbar_wait(LRing<false>::empty(bar0, j % 4), (j / 4) & 1u, abort_flag, p.wait_ns, p.status);
+        constexpr int S = LRing<false>::STAGES;
+        for (int j = (g > S ? g - S : 0); j < g && ok; ++j)
+          ok = mbar_wait(LRing<false>::empty(bar0, j % S), (j / S) & 1u, abort_flag, p.wait_ns, p.status);
         on_half = ok;
         for (; u < p.units && ok; u += G) {
           int tile, half;
@@ -225,11 +248,13 @@ __global__ void __launch_bounds__(LCfg::THREADS, 1) a4w4_large_kernel(const Larg
       }
       // every copy issued lands before the CTA's shared memory is released
       if (on_half) {
-        for (int j = (gh > 6 ? gh - 6 : 0); j < gh; ++j)
-          mbar_wait(LRing<true>::full(bar0, j % 6), (j / 6) & 1u, never, drain_ns, p.status);
+        constexpr int S = LRing<true>::STAGES;
+        for (int j = (gh > S ? gh - S : 0); j < gh; ++j)
+          mbar_wait(LRing<true>::full(bar0, j % S), (j / S) & 1u, never, drain_ns, p.status);
       } else {
-        for (int j = (g > 4 ? g - 4 : 0); j < g; ++j)
-          mbar_wait(LRing<false>::full(bar0, j % 4), (j / 4) & 1u, never, drain_ns, p.status);
+        constexpr int S = LRing<false>::STAGES;
+        for (int j = (g > S ? g - S : 0); j < g; ++j)
+          mbar_wait(LRing<false>::full(bar0, j % S), (j / S) & 1u, never, drain_ns, p.status);
       }
     }
   } else if (warp == 1) {
