@@ -83,8 +83,8 @@ def test_ragged_m_spans_tiles(M):
                                    # persistent large-M walk: two tiles per CTA and a ragged last row
                                    # tile; a last partial wave run as 128-column halves after a full tile;
                                    # K = 128, one K tile half of which is padding; the switch from the
-                                   # 4-deep whole-tile ring to the 6-deep half-unit ring after 5 K tiles
-                                   # (not a multiple of either depth)
+                                   # whole-tile ring (4 stages of one K tile) to the half-unit ring (3
+                                   # stages of two K tiles) after 5 K tiles, the last half stage single
                                    (1100, 8192, 512), (1200, 4096, 512), (1100, 8192, 128),
                                    (1200, 4096, 1280)])
 def test_k_tails_and_shapes(M, N, K):
