@@ -688,18 +688,27 @@ GemmPlan plan_gemm(int M, int N, int K, int sms) {
   if (M <= 16 || (M <= 32 && (pl.kt <= 4 || decode_splits(pl.kt, 4, N / 128, sms) > kMaxClusterSplits))) {
     // Decode kernel (decode.cu), no workspace.  16 tokens: 3 CTAs fit per SM,
     // so a 3-deep ring (room for the next grid's CTAs to start early and
-    // stream their weights), 4 deep when 3 would need over 16 splits.  32
-    // tokens fit 2 per SM (4-deep ring); the swap-AB kernel reduces their
-    // 16 KB split-K partials as fast, so they come here only when one CTA
-    // holds the whole K range or when 16-wide clusters give the grid more
-    // CTAs than its 8-wide ones.
+    // stream their weights), 4 deep when 3 would need over 16 splits.  17-32
+    // tokens whose whole K range fits one CTA's ring (K <= 1024) run as two
+    // 16-token tiles, each CTA quantising half the rows (32x7168x768: 4.8
+    // against 5.6 us in one 32-token tile).  Otherwise 32 tokens fit 2 per SM
+    // (4-deep ring); the swap-AB kernel reduces their 16 KB split-K partials
+    // as fast, so they come here only when 16-wide clusters give the grid
+    // more CTAs than its 8-wide ones (two 16-token tiles with split-K read
+    // every weight byte twice: 14.3 against 10.4 us at 32x7168x4224).
     pl.swap_ab = 1;
     pl.decode = 1;
-    pl.nx = M <= 16 ? 16 : 32;
     pl.w_tiles = N / 128;
-    pl.x_tiles = 1;
-    pl.ring = (pl.nx == 16 && (pl.kt + 2) / 3 <= kMaxDecodeSplits) ? 3 : 4;
-    pl.splits = decode_splits(pl.kt, pl.ring, pl.w_tiles, sms);
+    if (M <= 16 || pl.kt <= 4) {
+      pl.nx = 16;
+      pl.x_tiles = (M + 15) / 16;
+      pl.ring = M > 16 ? (pl.kt <= 3 ? 3 : 4) : ((pl.kt + 2) / 3 <= kMaxDecodeSplits ? 3 : 4);
+    } else {
+      pl.nx = 32;
+      pl.x_tiles = 1;
+      pl.ring = 4;
+    }
+    pl.splits = decode_splits(pl.kt, pl.ring, pl.w_tiles * pl.x_tiles, sms);
     pl.cluster_reduce = pl.splits > 1;
     return pl;
   }

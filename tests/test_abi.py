@@ -64,7 +64,8 @@ def test_kernel_routing_of_the_workload_shapes():
             assert name(M, N, K) == "a4w4_decode_kernel<16,3>"
     assert name(32, 7168, 4224) == "a4w4_gemm_kernel<swap,32>"      # 5 splits: swap-AB's clusters suffice
     assert name(32, 1536, 7168) == "a4w4_decode_kernel<32,4>"       # 16 splits fill the grid
-    assert name(32, 7168, 768) == "a4w4_decode_kernel<32,4>"        # one CTA holds the K range
+    assert name(32, 7168, 768) == "a4w4_decode_kernel<16,3>"        # one CTA holds the K range: two 16-token tiles
+    assert name(20, 1536, 1024) == "a4w4_decode_kernel<16,4>"
     assert name(1, 256, 16384 * 4) == "a4w4_decode_kernel<16,4>"    # a 3-deep ring would need > 16 splits
     assert name(37, 1536, 4224) == "a4w4_gemm_kernel<swap,64>"
     assert name(100, 1536, 4224) == "a4w4_gemm_kernel<swap,128>"     # N < 4096: swap-AB up to 128 tokens

@@ -76,6 +76,8 @@ DENSE_CASES = [
     (8, 1536, 7168, "decode"),      # decode kernel, 16 K splits
     (16, 7168, 768, "decode"),      # decode kernel, one CTA holds K
     (32, 1536, 7168, "decode"),     # decode kernel, 32-token tile
+    (32, 7168, 768, "decode"),      # decode kernel, two 16-token tiles (one CTA holds K)
+    (24, 1536, 1024, "stress"),     # two 16-token tiles, the second ragged; 4-deep ring
     (32, 7168, 4224, "decode"),     # swap-AB, 32-token tile
     (1, 1536, 4224, "stress"),      # M tails on the scale-edge blocks
     (17, 1536, 4224, "stress"),
