@@ -262,14 +262,12 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Sign bits of the 8 BF16 elements held in w[0..3] placed at bit 4i+3.
-__device__ __forceinline__ uint32_t bf16x8_signs(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-  return ((w0 >> 12) & 0x8u) | ((w0 >> 24) & 0x80u) | ((w1 >> 4) & 0x800u) | ((w1 >> 16) & 0x8000u) |
-         ((w2 << 4) & 0x80000u) | ((w2 >> 8) & 0x800000u) | ((w3 << 12) & 0x8000000u) | (w3 & 0x80000000u);
-}
-
 // x: 32 BF16 values as 16 words (element 2j in the low half of w[j]).
-// Returns the E8M0 code; codes[0..3] receive the 16 packed code bytes.
+// Returns the E8M0 code; codes[0..3] receive the 16 packed code bytes.  The
+// signed values go through the conversion as they are: E2M1 is
+// sign-magnitude and round-to-nearest-even and saturation are symmetric, so
+// the code of -x is the code of x with bit 3 set, a negative value that
+// rounds to zero included (code 8), as the rule wants.
 __device__ __forceinline__ uint32_t quant32_bf16(const uint32_t* w, uint32_t* codes) {
   uint32_t m = 0;
 #pragma unroll
@@ -283,12 +281,11 @@ __device__ __forceinline__ uint32_t quant32_bf16(const uint32_t* w, uint32_t* co
     float y[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t a = w[4 * q + j] & 0x7FFF7FFFu;
+      const uint32_t a = w[4 * q + j];
       y[2 * j] = __uint_as_float(a << 16) * inv;
       y[2 * j + 1] = __uint_as_float(a & 0xFFFF0000u) * inv;
     }
-    codes[q] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]) |
-               bf16x8_signs(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    codes[q] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
   }
   return code;
 }
