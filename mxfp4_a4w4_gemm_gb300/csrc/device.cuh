@@ -256,11 +256,14 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float y0, float y1, float y2, flo
   return w;
 }
 
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+// Per 16-bit lane: the BF16 value of larger magnitude, with its sign replaced
+// by the xor of the two inputs' signs.
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
+
 
 // x: 32 BF16 values as 16 words (element 2j in the low half of w[j]).
 // Returns the E8M0 code; codes[0..3] receive the 16 packed code bytes.  The
@@ -269,9 +272,13 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // the code of -x is the code of x with bit 3 set, a negative value that
 // rounds to zero included (code 8), as the rule wants.
 __device__ __forceinline__ uint32_t quant32_bf16(const uint32_t* w, uint32_t* codes) {
-  uint32_t m = 0;
+  // the larger magnitude of each BF16 lane pair, one instruction per word
+  // (finite inputs: magnitude order is the order of the unsigned bit patterns
+  // with the sign cleared; the result's sign bits are dropped below)
+  uint32_t m = w[0];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) m = max_u16x2(m, w[j] & 0x7FFF7FFFu);
+  for (int j = 1; j < 16; ++j) m = max_abs_bf16x2(m, w[j]);
+  m &= 0x7FFF7FFFu;
   const uint32_t amax = max(m & 0xFFFFu, m >> 16);
   const uint32_t ebits = amax >> 7;
   const uint32_t code = ebits > 2u ? ebits - 2u : 0u;
