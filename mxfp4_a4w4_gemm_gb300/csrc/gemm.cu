@@ -412,18 +412,29 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
         fence_proxy_async_smem();
         mbar_arrive(full_x(s));
       };
-      uint4 ca[PER], cb[PER];
-      uint32_t ea[PER], eb[PER];
-      if (nq > 0) gload(0, ca, ea);
-      for (int i = 0; i < nq; i += 2) {
-        if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        if (i + 1 < nq) gload(i + 1, cb, eb);
-        gstore(i, ca, ea);
-        if (i + 1 >= nq) break;
-        const int i1 = i + 1;
-        if (!mbar_wait(empty(i1 % STAGES), ((i1 / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) break;
-        if (i1 + 1 < nq) gload(i1 + 1, ca, ea);
-        gstore(i1, cb, eb);
+      // a register ring of GQ stages: the gathers of stages i+1 .. i+GQ-1 are
+      // in flight while stage i is stored (full expert blocks gather 16 KB of
+      // scattered rows per stage; one stage ahead left each stage waiting on
+      // most of an L2 round trip)
+      constexpr int GQ = 3;
+      uint4 cq[GQ][PER];
+      uint32_t eq[GQ][PER];
+#pragma unroll
+      for (int r = 0; r < GQ; ++r)
+        if (r < nq) gload(r, cq[r], eq[r]);
+      bool stop = false;
+      for (int i0 = 0; i0 < nq && !stop; i0 += GQ) {
+#pragma unroll
+        for (int r = 0; r < GQ; ++r) {
+          const int i = i0 + r;
+          if (i >= nq) break;
+          if (!mbar_wait(empty(i % STAGES), ((i / STAGES) & 1) ^ 1u, abort_flag, p.wait_ns, p.status)) {
+            stop = true;
+            break;
+          }
+          gstore(i, cq[r], eq[r]);
+          if (i + GQ < nq) gload(i + GQ, cq[r], eq[r]);
+        }
       }
     } else if (PER <= 2) {
       // A register ring: the loads of stages i+1 .. i+R-1 are in flight while
