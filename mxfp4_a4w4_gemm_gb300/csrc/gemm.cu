@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(Cfg<MODE, NX, STAGES>::THREADS, Cfg<MODE, NX, 
     if constexpr (Cf::kGatherQ) {
       // Rows were quantised once beforehand (codes [T, K/2], scales [T, K/32]):
       // copy this thread's 16-byte code chunks and scale bytes of a stage into
-      // the swizzled tile and the scale atom; loads one stage ahead.
+      // the swizzled tile and the scale atom; loads run ahead of the stores in
+      // a register ring (below).
       auto gload = [&](int i, uint4 (&c)[PER], uint32_t (&e)[PER]) {
 #pragma unroll
         for (int u = 0; u < PER; ++u) {

@@ -83,7 +83,7 @@ DENSE_CASES = [
     (17, 1536, 4224, "stress"),
     (37, 1536, 4224, "stress"),     # swap-AB, 64-token tile
     (100, 1536, 4224, "stress"),    # swap-AB, 128-token tile
-    (65, 7168, 4224, "stress"),     # quantise-once pre-pass, one tile, valid-row count
+    (65, 7168, 4224, "stress"),     # quantise-once pre-pass, one tile, rows past M zero
     (513, 1536, 4224, "stress"),    # quantise-once pre-pass, ragged last tile
     (2047, 1536, 4224, "stress"),
 ]
